@@ -1,0 +1,29 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built libfcp.so")
+
+
+@pytest.fixture(scope="session")
+def lib():
+    """The C-ABI library, built in-tree on first use."""
+    from context_document_masked_gb300 import build as b
+    b.ensure_built()
+    from context_document_masked_gb300 import fcp
+    return fcp
+
+
+@pytest.fixture(scope="session")
+def cuda():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch.device("cuda:0")
