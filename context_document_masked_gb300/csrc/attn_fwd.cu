@@ -1,0 +1,497 @@
+// Document-masked attention forward on sm_103a (tcgen05 + TMA + TMEM).
+//
+// Computes, for every query row i of the selected shard(s) and query head h,
+//   s_ij = scale <q_ih, k_jg>   over keys j of doc(i) with j <= i,
+//   LSE_ih = ln sum_j exp(s_ij),  O_ih = sum_j exp(s_ij - LSE_ih) v_jg
+// ("FlashCP: Load-Balanced Communication-Efficient Context Parallelism for
+// LLM Training", §2.1 and Fig. 1(a): the intra-document causal mask), with
+// the keys a shard needs read from its own rows of K/V and from the
+// compacted buffer of received prefix keys (§3.2). The softmax is evaluated
+// online, keeping a running row maximum and exponential sum ("LLM Context
+// Parallel in Production", "Core Principle: Split Q, Circulate KV").
+//
+// Work unit: one 128-row query tile of one piece (a shard's query range inside
+// one document) for TWO query heads of the same GQA group, which read the
+// same K/V tiles. Key tiles are 128 keys of one key segment (a run of keys
+// held by the shard or received from others), so only tiles that contain
+// useful (q, k) pairs are visited; tiles on the diagonal or at a segment end
+// are masked element by element.
+//
+// CTA roles (384 threads, persistent over the work list):
+//   warp 0      TMA producer: Q tiles of both heads, then K/V tiles into a
+//               ring of shared-memory stages.
+//   warp 1      MMA issuer (one thread): S_i = Q_i K^T and O_i += P_i V with
+//               tcgen05.mma, accumulators in TMEM; allocates TMEM.
+//   warps 4-7   softmax for head 0 of the pair, warps 8-11 for head 1: read
+//               S from TMEM (one row per thread), mask, update the running
+//               max / sum, write P (fp16) to shared memory, rescale O in TMEM
+//               when the max grows by more than 2^8, and finish the rows.
+// Q K^T runs on the bf16 inputs; P V runs on fp16 operands (P <= 2^8 after
+// the lazy rescale, V from an fp16 copy), whose 11 significant bits keep the
+// rounding of P four times below bf16's.
+// The two heads ping-pong: while one softmax group works on its S, the
+// tensor core runs the other head's P*V and next S.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+#include "sm103.cuh"
+
+namespace fcp {
+
+using namespace dev;
+
+namespace {
+
+constexpr int kThreads = 384;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kStages = D == 128 ? 3 : 6;
+  static constexpr int kPanels = D / 64;                 // 64-column swizzle panels per row
+  static constexpr int kTileBytes = 128 * D * 2;         // one Q/K/V tile
+  static constexpr int kPBytes = 128 * 128 * 2;
+  static constexpr int kQOff = 0;
+  static constexpr int kKVOff = 2 * kTileBytes;
+  static constexpr int kPOff = kKVOff + kStages * kTileBytes;
+  static constexpr int kSmem = kPOff + 2 * kPBytes;
+  static constexpr int kSmemAlloc = kSmem + 1024;        // slack for 1024-byte alignment
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColS = 0;                   // S_i at i*128
+  static constexpr uint32_t kColO = 256;                 // O_i at 256 + i*D
+};
+
+// Key tiles of one query tile: every segment of the piece, clipped to the key
+// block [lo, hi) and to keys <= q_last, cut into tiles of 128 keys.
+struct Walker {
+  const int32_t* seg;
+  int s, s_end, q_last, lo, hi, shift;
+  int pos, end, ks, src, srow;
+
+  __device__ void init(const int32_t* segs, int seg_begin, int seg_count, int q_last_, int lo_,
+                       int hi_, int shift_) {
+    seg = segs;
+    s = seg_begin - 1;
+    s_end = seg_begin + seg_count;
+    q_last = q_last_;
+    lo = lo_;
+    hi = hi_;
+    shift = shift_;
+    pos = end = 0;
+  }
+  __device__ bool next(int& src_o, int& row_o, int& key_o, int& n_o) {
+    while (pos >= end) {
+      if (++s >= s_end) return false;
+      const int* g = seg + 4 * s;
+      ks = __ldg(g + 2);
+      if (ks > q_last) {
+        s = s_end;
+        return false;
+      }
+      const int len = __ldg(g + 3);
+      src = __ldg(g + 0);
+      srow = __ldg(g + 1) - (src ? shift : 0);
+      pos = max(ks, lo);
+      end = min(min(ks + len, hi), q_last + 1);
+    }
+    src_o = src;
+    row_o = srow + (pos - ks);
+    key_o = pos;
+    n_o = min(128, end - pos);
+    pos += 128;
+    return true;
+  }
+};
+
+__device__ __forceinline__ int count_key_tiles(const int32_t* segs, int seg_begin, int seg_count,
+                                               int q_last, int lo, int hi) {
+  int n = 0;
+  for (int s = seg_begin; s < seg_begin + seg_count; ++s) {
+    const int* g = segs + 4 * s;
+    const int ks = __ldg(g + 2);
+    if (ks > q_last) break;
+    const int a = max(ks, lo);
+    const int e = min(min(ks + __ldg(g + 3), hi), q_last + 1);
+    if (e > a) n += (e - a + 127) / 128;
+  }
+  return n;
+}
+
+struct WorkItem {
+  int q_start, q_rows, seg_begin, seg_count, h0, g;
+};
+
+__device__ __forceinline__ WorkItem decode(const FwdParams& p, int w) {
+  const int hp_count = p.hq / 2;
+  const int item = __ldg(p.order + w / hp_count);
+  const int hp = w % hp_count;
+  const int* t = p.tiles + 4 * item;
+  const int piece = __ldg(t + 0);
+  WorkItem it;
+  it.q_start = __ldg(t + 1);
+  it.q_rows = __ldg(t + 2);
+  it.seg_begin = __ldg(p.pieces + 8 * piece + 5);
+  it.seg_count = __ldg(p.pieces + 8 * piece + 6);
+  it.h0 = 2 * hp;
+  it.g = it.h0 / (p.hq / p.hkv);
+  return it;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kb,
+                    const __grid_constant__ CUtensorMap tm_vb, const FwdParams p) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t bar_q_full, bar_q_empty, bar_drain;
+  __shared__ __align__(8) uint64_t bar_kv_full[C::kStages], bar_kv_empty[C::kStages];
+  __shared__ __align__(8) uint64_t bar_s_full[2], bar_p_ready[2], bar_o_done[2], bar_o_free[2];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  if (tid == 0) {
+    mbar_init(&bar_q_full, 1);
+    mbar_init(&bar_q_empty, 1);
+    mbar_init(&bar_drain, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&bar_kv_full[s], 1);
+      mbar_init(&bar_kv_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_s_full[i], 1);
+      mbar_init(&bar_p_ready[i], 128);
+      mbar_init(&bar_o_done[i], 1);
+      mbar_init(&bar_o_free[i], 128);
+    }
+    abort_sh = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, C::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+    prefetch_tmap(&tm_kb);
+    prefetch_tmap(&tm_vb);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  const WaitCtl wc{&abort_sh, p.err, p.wait_ns};
+  const int n_work = p.n_items * (p.hq / 2);
+
+  uint8_t* sQ = smem + C::kQOff;
+  uint8_t* sKV = smem + C::kKVOff;
+  uint8_t* sP = smem + C::kPOff;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t kv_cnt = 0, q_iter = 0;
+      uint32_t issued[C::kStages];
+      for (int s = 0; s < C::kStages; ++s) issued[s] = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
+        const WorkItem it = decode(p, w);
+        const int q_last = it.q_start + it.q_rows - 1;
+        const int nt = count_key_tiles(p.segs, it.seg_begin, it.seg_count, q_last, p.kv_lo, p.kv_hi);
+        if (nt == 0) continue;
+        if (q_iter > 0 && !(ok = mbar_wait(&bar_q_empty, (q_iter - 1) & 1, wc))) break;
+        mbar_arrive_expect_tx(&bar_q_full, 2 * C::kTileBytes);
+        for (int h = 0; h < 2; ++h)
+          for (int pn = 0; pn < C::kPanels; ++pn)
+            tma_load_3d(sQ + h * C::kTileBytes + pn * 16384, &tm_q, &bar_q_full, pn * 64, it.h0 + h,
+                        it.q_start);
+        ++q_iter;
+        Walker wk;
+        wk.init(p.segs, it.seg_begin, it.seg_count, q_last, p.kv_lo, p.kv_hi, p.kbuf_shift);
+        int src, row, key, n;
+        while (ok && wk.next(src, row, key, n)) {
+          for (int kv = 0; kv < 2; ++kv) {
+            const int s = kv_cnt % C::kStages;
+            if (kv_cnt >= (uint32_t)C::kStages &&
+                !(ok = mbar_wait(&bar_kv_empty[s], ((kv_cnt / C::kStages) - 1) & 1, wc)))
+              break;
+            mbar_arrive_expect_tx(&bar_kv_full[s], C::kTileBytes);
+            const CUtensorMap* tm = kv == 0 ? (src ? &tm_kb : &tm_k) : (src ? &tm_vb : &tm_v);
+            for (int pn = 0; pn < C::kPanels; ++pn)
+              tma_load_3d(sKV + s * C::kTileBytes + pn * 16384, tm, &bar_kv_full[s], pn * 64, it.g,
+                          row);
+            ++issued[s];
+            ++kv_cnt;
+          }
+        }
+      }
+      // Every copy this thread started has landed before the CTA exits.
+      for (int s = 0; s < C::kStages; ++s)
+        if (issued[s]) mbar_drain(&bar_kv_full[s], (issued[s] - 1) & 1);
+      if (q_iter) mbar_drain(&bar_q_full, (q_iter - 1) & 1);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idesc_o = idesc_f16kind(128, D, false, true, false);  // fp16 P, V
+      uint32_t kv_cnt = 0, q_iter = 0, items = 0;
+      uint32_t p_cnt[2] = {0, 0};
+      bool ok = true;
+      const uint32_t q_base = smem_u32(sQ);
+      const uint32_t kv_base = smem_u32(sKV);
+      const uint32_t p_base = smem_u32(sP);
+      auto issue_s = [&](int i, uint32_t kstage) {
+        const uint32_t qa = q_base + i * C::kTileBytes;
+        const uint32_t ka = kv_base + kstage * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_bf16_ss(tmem + C::kColS + i * 128, smem_desc_sw128(qa + off, 0, 1024),
+                      smem_desc_sw128(ka + off, 0, 1024), idesc_s, kk > 0);
+        }
+      };
+      auto issue_o = [&](int i, uint32_t vstage, bool acc) {
+        const uint32_t pa = p_base + i * C::kPBytes;
+        const uint32_t va = kv_base + vstage * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_bf16_ss(tmem + C::kColO + i * D, smem_desc_sw128(pa + aoff, 0, 1024),
+                      smem_desc_sw128(va + kk * 2048, 16384, 1024), idesc_o, (acc || kk > 0));
+        }
+      };
+      for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
+        const WorkItem it = decode(p, w);
+        const int q_last = it.q_start + it.q_rows - 1;
+        const int nt = count_key_tiles(p.segs, it.seg_begin, it.seg_count, q_last, p.kv_lo, p.kv_hi);
+        if (nt == 0) continue;
+        if (!(ok = mbar_wait(&bar_q_full, q_iter & 1, wc))) break;
+        tc_fence_after();
+        // S_0, S_1 of the first key tile.
+        {
+          const uint32_t c = kv_cnt, s = c % C::kStages;
+          if (!(ok = mbar_wait(&bar_kv_full[s], (c / C::kStages) & 1, wc))) break;
+          tc_fence_after();
+          issue_s(0, s);
+          mma_commit(&bar_s_full[0]);
+          issue_s(1, s);
+          mma_commit(&bar_s_full[1]);
+          mma_commit(&bar_kv_empty[s]);
+        }
+        for (int t = 0; t < nt && ok; ++t) {
+          const uint32_t cv = kv_cnt + 2 * t + 1, sv = cv % C::kStages;
+          if (!(ok = mbar_wait(&bar_kv_full[sv], (cv / C::kStages) & 1, wc))) break;
+          for (int i = 0; i < 2; ++i) {
+            if (!(ok = mbar_wait(&bar_p_ready[i], p_cnt[i] & 1, wc))) break;
+            ++p_cnt[i];
+            if (t == 0 && items > 0 && !(ok = mbar_wait(&bar_o_free[i], (items - 1) & 1, wc))) break;
+            tc_fence_after();
+            issue_o(i, sv, t > 0);
+            mma_commit(&bar_o_done[i]);
+            if (i == 1) mma_commit(&bar_kv_empty[sv]);
+            if (t + 1 < nt) {
+              const uint32_t ck = kv_cnt + 2 * (t + 1), sk = ck % C::kStages;
+              if (!(ok = mbar_wait(&bar_kv_full[sk], (ck / C::kStages) & 1, wc))) break;
+              tc_fence_after();
+              issue_s(i, sk);
+              mma_commit(&bar_s_full[i]);
+              if (i == 1) mma_commit(&bar_kv_empty[sk]);
+            }
+          }
+        }
+        if (!ok) break;
+        mma_commit(&bar_q_empty);
+        kv_cnt += 2 * nt;
+        ++q_iter;
+        ++items;
+      }
+      // Every MMA this thread issued has finished before TMEM is released.
+      mma_commit(&bar_drain);
+      mbar_drain(&bar_drain, 0);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    const int i = (warp - 4) >> 2;          // which head of the pair
+    const int r = tid - 128 * (1 + i);      // tile row == TMEM lane
+    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t s_col = lane_base + C::kColS + i * 128;
+    const uint32_t o_col = lane_base + C::kColO + i * D;
+    const uint32_t p_row = smem_u32(sP + i * C::kPBytes);
+    uint32_t s_cnt = 0, o_cnt = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
+      const WorkItem it = decode(p, w);
+      const int q_last = it.q_start + it.q_rows - 1;
+      const int nt = count_key_tiles(p.segs, it.seg_begin, it.seg_count, q_last, p.kv_lo, p.kv_hi);
+      const int q = it.q_start + r;
+      const bool row_valid = r < it.q_rows;
+      const int head = it.h0 + i;
+      float m_run = -INFINITY, l = 0.f;
+      if (nt > 0) {
+        Walker wk;
+        wk.init(p.segs, it.seg_begin, it.seg_count, q_last, p.kv_lo, p.kv_hi, p.kbuf_shift);
+        int src, row, key, n;
+        for (int t = 0; t < nt; ++t) {
+          wk.next(src, row, key, n);
+          ok = mbar_wait(&bar_s_full[i], s_cnt & 1, wc);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          ++s_cnt;
+          tc_fence_after();
+          float s[128];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            float v[32];
+            tmem_ld32(s_col + c * 32, v);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) s[c * 32 + j] = v[j];
+          }
+          tmem_ld_wait();
+          if (key + 127 > it.q_start || n < 128) {
+            const int lim = min(n, q - key + 1);  // keys [key, key+lim) are visible to row q
+#pragma unroll
+            for (int c = 0; c < 128; ++c)
+              if (c >= lim) s[c] = -INFINITY;
+          }
+          float mx = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < 128; ++c) mx = fmaxf(mx, s[c]);
+          mx *= p.scale_log2;
+          const float m_new = fmaxf(m_run, mx);
+          const bool rescale = m_new > m_run + kRescaleThreshold;
+          float alpha = 1.f;
+          if (rescale) {
+            alpha = ex2(m_run - m_new);
+            m_run = m_new;
+          }
+          const float m_use = m_run == -INFINITY ? 0.f : m_run;
+          float rowsum = 0.f;
+#pragma unroll
+          for (int c = 0; c < 128; ++c) {
+            s[c] = ex2(fmaf(s[c], p.scale_log2, -m_use));
+            rowsum += s[c];
+          }
+          if (t > 0) {
+            // P buffer and O accumulator are free once P*V of the previous tile is done.
+            ok = mbar_wait(&bar_o_done[i], o_cnt & 1, wc);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            ++o_cnt;
+            tc_fence_after();
+            if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+              for (int c = 0; c < D / 32; ++c) {
+                float v[32];
+                tmem_ld32(o_col + c * 32, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] *= alpha;
+                tmem_st32(o_col + c * 32, v);
+              }
+              tmem_st_wait();
+            }
+          }
+          l = l * alpha + rowsum;
+          // P row r -> shared memory, two 64-key swizzled panels.
+#pragma unroll
+          for (int ch = 0; ch < 16; ++ch) {
+            const int c0 = ch * 8;
+            const uint32_t addr = p_row + (ch >> 3) * 16384 + sw128_offset(r, ch & 7);
+            st_shared_v4(addr, pack_f16(s[c0], s[c0 + 1]), pack_f16(s[c0 + 2], s[c0 + 3]),
+                         pack_f16(s[c0 + 4], s[c0 + 5]), pack_f16(s[c0 + 6], s[c0 + 7]));
+          }
+          fence_proxy_async_smem();
+          tc_fence_before();
+          mbar_arrive(&bar_p_ready[i]);
+        }
+        if (!ok) break;
+        ok = mbar_wait(&bar_o_done[i], o_cnt & 1, wc);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        ++o_cnt;
+        tc_fence_after();
+      }
+      // Epilogue: O / l and LSE for this row.
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const size_t obase = ((size_t)q * p.hq + head) * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        float v[32];
+        if (nt > 0) {
+          tmem_ld32(o_col + c * 32, v);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = 0.f;
+        }
+        if (row_valid) {
+          if (p.out_f32) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + obase + c * 32);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              dst[j] = make_float4(v[4 * j] * inv, v[4 * j + 1] * inv, v[4 * j + 2] * inv,
+                                   v[4 * j + 3] * inv);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + obase + c * 32);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              dst[j] = make_uint4(pack_bf16(v[8 * j] * inv, v[8 * j + 1] * inv),
+                                  pack_bf16(v[8 * j + 2] * inv, v[8 * j + 3] * inv),
+                                  pack_bf16(v[8 * j + 4] * inv, v[8 * j + 5] * inv),
+                                  pack_bf16(v[8 * j + 6] * inv, v[8 * j + 7] * inv));
+          }
+        }
+      }
+      if (row_valid)
+        p.lse[(size_t)head * p.T + q] = l > 0.f ? (m_run + log2f(l)) * 0.69314718055994531f : -INFINITY;
+      if (nt > 0) {
+        tc_fence_before();
+        mbar_arrive(&bar_o_free[i]);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+}  // namespace
+
+template <int D>
+static int launch_fwd_impl(const FwdLaunch& a, cudaStream_t st) {
+  using C = FwdCfg<D>;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemAlloc) != cudaSuccess)
+      return FCP_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  const int n_work = a.p.n_items * (a.p.hq / 2);
+  if (n_work == 0) return FCP_OK;
+  const int grid = n_work < a.num_sms ? n_work : a.num_sms;
+  attn_fwd_kernel<D><<<grid, kThreads, C::kSmemAlloc, st>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_kb, a.tm_vb,
+                                                           a.p);
+  return cudaGetLastError() == cudaSuccess ? FCP_OK : FCP_ERR_CUDA;
+}
+
+int launch_attn_fwd(const FwdLaunch& a, cudaStream_t st) {
+  if (a.d == 128) return launch_fwd_impl<128>(a, st);
+  if (a.d == 64) return launch_fwd_impl<64>(a, st);
+  return FCP_ERR_UNSUPPORTED;
+}
+
+}  // namespace fcp

@@ -1,0 +1,297 @@
+// Bandwidth-bound kernels of libfcp: the sharding-aware KV gather, the
+// (O, LSE) merge of partial results, and the backward row statistics.
+//
+// All three move contiguous rows with 128-bit loads and stores, several
+// independent loads in flight per thread, and grids sized in multiples of the
+// SM count.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+
+namespace fcp {
+
+namespace {
+
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ------------------------------------------------------------------ gather
+// "FlashCP" §3.2: each shard receives only the prefix keys of its documents
+// held by other shards, compacted into one contiguous buffer. A task copies
+// `nrows` consecutive rows (contiguous in source and destination) of K and V.
+constexpr int kGatherThreads = 256;
+constexpr int kGatherUnroll = 4;
+
+__global__ void __launch_bounds__(kGatherThreads)
+    gather_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+                  const int32_t* __restrict__ tasks, int32_t n_tasks, int32_t dst_shift,
+                  int64_t row_vecs, uint4* __restrict__ kbuf, uint4* __restrict__ vbuf) {
+  for (int t = blockIdx.x; t < n_tasks; t += gridDim.x) {
+    const int src = __ldg(tasks + 4 * t + 0);
+    const int dst = __ldg(tasks + 4 * t + 1) - dst_shift;
+    const int nrows = __ldg(tasks + 4 * t + 2);
+    const int64_t n = (int64_t)nrows * row_vecs;
+    const uint4* ks = k + (int64_t)src * row_vecs;
+    const uint4* vs = v + (int64_t)src * row_vecs;
+    uint4* kd = kbuf + (int64_t)dst * row_vecs;
+    uint4* vd = vbuf + (int64_t)dst * row_vecs;
+    const int64_t step = (int64_t)kGatherThreads * kGatherUnroll;
+    for (int64_t base = threadIdx.x; base < n; base += step) {
+      uint4 a[kGatherUnroll], b[kGatherUnroll];
+#pragma unroll
+      for (int u = 0; u < kGatherUnroll; ++u) {
+        const int64_t i = base + (int64_t)u * kGatherThreads;
+        if (i < n) {
+          a[u] = __ldg(ks + i);
+          b[u] = __ldg(vs + i);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kGatherUnroll; ++u) {
+        const int64_t i = base + (int64_t)u * kGatherThreads;
+        if (i < n) {
+          kd[i] = a[u];
+          vd[i] = b[u];
+        }
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------- merge
+// "LLM Context Parallel in Production", "Core Principle" / "Ring Attention":
+// LSE = ln sum_b exp(LSE_b), O = sum_b exp(LSE_b - LSE) O_b. One thread owns
+// four consecutive head-dim elements of one (row, head); parts whose LSE is
+// -inf (no key of that block visible) are not read.
+constexpr int kMergeThreads = 256;
+
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads)
+    merge_kernel(const float4* __restrict__ o_parts, const float* __restrict__ lse_parts, int B,
+                 int64_t rows, int hq, uint2* __restrict__ out, float* __restrict__ lse_out) {
+  constexpr int V = D / 4;  // float4 per (row, head)
+  const int64_t total = rows * hq * V;
+  const float kLog2e = 1.4426950408889634f;
+  for (int64_t idx = (int64_t)blockIdx.x * kMergeThreads + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * kMergeThreads) {
+    const int vec = (int)(idx % V);
+    const int64_t rh = idx / V;
+    const int h = (int)(rh % hq);
+    const int64_t row = rh / hq;
+    float m = -INFINITY;
+    for (int b = 0; b < B; ++b) m = fmaxf(m, __ldg(lse_parts + ((int64_t)b * hq + h) * rows + row));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float lse = -INFINITY;
+    if (m != -INFINITY) {
+      float total_w = 0.f;
+      for (int b = 0; b < B; ++b) {
+        const float lb = __ldg(lse_parts + ((int64_t)b * hq + h) * rows + row);
+        if (lb == -INFINITY) continue;
+        const float w = ex2f((lb - m) * kLog2e);
+        const float4 o = __ldg(o_parts + (((int64_t)b * rows + row) * hq + h) * V + vec);
+        total_w += w;
+        acc.x = fmaf(w, o.x, acc.x);
+        acc.y = fmaf(w, o.y, acc.y);
+        acc.z = fmaf(w, o.z, acc.z);
+        acc.w = fmaf(w, o.w, acc.w);
+      }
+      const float inv = 1.f / total_w;
+      acc.x *= inv;
+      acc.y *= inv;
+      acc.z *= inv;
+      acc.w *= inv;
+      lse = m + logf(total_w);
+    }
+    out[(row * hq + h) * V + vec] = make_uint2(pack2(acc.x, acc.y), pack2(acc.z, acc.w));
+    if (vec == 0) lse_out[(int64_t)h * rows + row] = lse;
+  }
+}
+
+// ------------------------------------------------------- bwd preprocess
+// D_i = <dO_i, O_i> (the row term of dS = P (dP - D)), dQ rows zeroed so the
+// backward kernel can accumulate into them, and fp16 copies of Q and dO (the
+// backward's tensor-core operands; exact for bf16 values inside the fp16
+// range, error bit 4 otherwise). One warp per (row, head).
+constexpr int kPreThreads = 256;
+
+__device__ __forceinline__ uint32_t cvt_pair(uint32_t x, bool& ovf) {
+  const float lo = __uint_as_float(x << 16), hi = __uint_as_float(x & 0xFFFF0000u);
+  ovf |= fabsf(lo) > 65504.f || fabsf(hi) > 65504.f;
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// The forward output O, as bf16 or fp32: four (or two) consecutive elements
+// of one row, widened to fp32.
+template <int E, bool F32>
+__device__ __forceinline__ void load_o(const void* out, int64_t base, float (&o)[E]) {
+  if constexpr (F32) {
+    const float* p = static_cast<const float*>(out) + base;
+    if constexpr (E == 4) {
+      const float4 x = *reinterpret_cast<const float4*>(p);
+      o[0] = x.x; o[1] = x.y; o[2] = x.z; o[3] = x.w;
+    } else {
+      const float2 x = *reinterpret_cast<const float2*>(p);
+      o[0] = x.x; o[1] = x.y;
+    }
+  } else {
+    const __nv_bfloat16* p = static_cast<const __nv_bfloat16*>(out) + base;
+    uint32_t w[E / 2];
+    if constexpr (E == 4) {
+      const uint2 x = *reinterpret_cast<const uint2*>(p);
+      w[0] = x.x; w[E / 2 - 1] = x.y;
+    } else {
+      w[0] = *reinterpret_cast<const uint32_t*>(p);
+    }
+#pragma unroll
+    for (int i = 0; i < E / 2; ++i) {
+      o[2 * i] = __uint_as_float(w[i] << 16);
+      o[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+}
+
+template <int D, bool OF32>
+__global__ void __launch_bounds__(kPreThreads)
+    preprocess_kernel(const void* __restrict__ out, const __nv_bfloat16* __restrict__ dout,
+                      const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ rows,
+                      const int32_t* __restrict__ order, int n_chunks, int T, int hq,
+                      float* __restrict__ delta, float* __restrict__ dq, __half* __restrict__ q16,
+                      __half* __restrict__ do16, int* __restrict__ err) {
+  constexpr int E = D / 32;  // elements per lane (4 or 2)
+  constexpr int W = E / 2;   // 32-bit words per lane
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  bool ovf = false;
+  for (int c = blockIdx.x; c < n_chunks; c += gridDim.x) {
+    const int chunk = __ldg(order + c);
+    const int r0 = __ldg(rows + 2 * chunk), nr = __ldg(rows + 2 * chunk + 1);
+    for (int pr = warp; pr < nr * hq; pr += kPreThreads / 32) {
+      const int r = r0 + pr / hq, h = pr % hq;
+      const int64_t base = ((int64_t)r * hq + h) * D + lane * E;
+      uint32_t b[W], x[W], oq[W], od[W];
+      float o[E];
+      load_o<E, OF32>(out, base, o);
+      if (W == 2) {
+        const uint2 vb = *reinterpret_cast<const uint2*>(dout + base);
+        const uint2 vx = *reinterpret_cast<const uint2*>(q + base);
+        b[0] = vb.x; b[W - 1] = vb.y; x[0] = vx.x; x[W - 1] = vx.y;
+      } else {
+        b[0] = *reinterpret_cast<const uint32_t*>(dout + base);
+        x[0] = *reinterpret_cast<const uint32_t*>(q + base);
+      }
+      float s = 0.f;
+#pragma unroll
+      for (int i = 0; i < W; ++i) {
+        s = fmaf(o[2 * i], __uint_as_float(b[i] << 16), s);
+        s = fmaf(o[2 * i + 1], __uint_as_float(b[i] & 0xFFFF0000u), s);
+        oq[i] = cvt_pair(x[i], ovf);
+        od[i] = cvt_pair(b[i], ovf);
+      }
+      if (W == 2) {
+        *reinterpret_cast<uint2*>(q16 + base) = make_uint2(oq[0], oq[W - 1]);
+        *reinterpret_cast<uint2*>(do16 + base) = make_uint2(od[0], od[W - 1]);
+        *reinterpret_cast<float4*>(dq + base) = make_float4(0.f, 0.f, 0.f, 0.f);
+      } else {
+        *reinterpret_cast<uint32_t*>(q16 + base) = oq[0];
+        *reinterpret_cast<uint32_t*>(do16 + base) = od[0];
+        *reinterpret_cast<float2*>(dq + base) = make_float2(0.f, 0.f);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (lane == 0) delta[(int64_t)h * T + r] = s;
+    }
+  }
+  if (ovf) atomicOr(err, 4);
+}
+
+// ------------------------------------------------------- bf16 -> fp16
+// fp16 copy of a bf16 tensor (exact inside the fp16 range; error bit 4 when a
+// value exceeds it). The forward's P*V product runs on fp16 operands.
+constexpr int kCvtThreads = 256;
+
+__global__ void __launch_bounds__(kCvtThreads)
+    convert_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t n, int* err) {
+  bool ovf = false;
+  for (int64_t i = (int64_t)blockIdx.x * kCvtThreads + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * kCvtThreads) {
+    uint4 x = __ldg(src + i);
+    x.x = cvt_pair(x.x, ovf);
+    x.y = cvt_pair(x.y, ovf);
+    x.z = cvt_pair(x.z, ovf);
+    x.w = cvt_pair(x.w, ovf);
+    dst[i] = x;
+  }
+  if (ovf) atomicOr(err, 4);
+}
+
+}  // namespace
+
+int launch_convert_f16(const void* src, void* dst, int64_t n_elems, int* err, int num_sms,
+                       cudaStream_t st) {
+  const int64_t n = n_elems / 8;
+  if (n == 0) return FCP_OK;
+  int64_t grid = (n + kCvtThreads - 1) / kCvtThreads;
+  if (grid > (int64_t)num_sms * 16) grid = (int64_t)num_sms * 16;
+  convert_kernel<<<(int)grid, kCvtThreads, 0, st>>>(static_cast<const uint4*>(src),
+                                                    static_cast<uint4*>(dst), n, err);
+  return cudaGetLastError() == cudaSuccess ? FCP_OK : FCP_ERR_CUDA;
+}
+
+int launch_gather(const void* k, const void* v, const int32_t* tasks, int32_t n_tasks,
+                  int32_t dst_shift, int64_t row_bytes, void* kbuf, void* vbuf, int num_sms,
+                  cudaStream_t st) {
+  if (n_tasks == 0) return FCP_OK;
+  const int grid = n_tasks < num_sms * 8 ? n_tasks : num_sms * 8;
+  gather_kernel<<<grid, kGatherThreads, 0, st>>>(
+      static_cast<const uint4*>(k), static_cast<const uint4*>(v), tasks, n_tasks, dst_shift,
+      row_bytes / 16, static_cast<uint4*>(kbuf), static_cast<uint4*>(vbuf));
+  return cudaGetLastError() == cudaSuccess ? FCP_OK : FCP_ERR_CUDA;
+}
+
+int launch_merge(const float* o_parts, const float* lse_parts, int32_t B, int64_t rows, int32_t hq,
+                 int32_t d, void* out, float* lse_out, int num_sms, cudaStream_t st) {
+  if (rows == 0) return FCP_OK;
+  const int64_t total = rows * hq * (d / 4);
+  int64_t grid = (total + kMergeThreads - 1) / kMergeThreads;
+  if (grid > (int64_t)num_sms * 64) grid = (int64_t)num_sms * 64;
+  if (d == 128)
+    merge_kernel<128><<<(int)grid, kMergeThreads, 0, st>>>(
+        reinterpret_cast<const float4*>(o_parts), lse_parts, B, rows, hq, static_cast<uint2*>(out),
+        lse_out);
+  else
+    merge_kernel<64><<<(int)grid, kMergeThreads, 0, st>>>(
+        reinterpret_cast<const float4*>(o_parts), lse_parts, B, rows, hq, static_cast<uint2*>(out),
+        lse_out);
+  return cudaGetLastError() == cudaSuccess ? FCP_OK : FCP_ERR_CUDA;
+}
+
+int launch_bwd_preprocess(const void* out, bool out_f32, const void* dout, const void* q,
+                          const int32_t* rows, const int32_t* order, int32_t n_chunks, int32_t T,
+                          int32_t hq, int32_t d, float* delta, float* dq, void* q16, void* do16,
+                          int* err, cudaStream_t st) {
+  if (n_chunks == 0) return FCP_OK;
+  const int grid = n_chunks;
+  using B = __nv_bfloat16;
+  auto go = [&](auto kernel) {
+    kernel<<<grid, kPreThreads, 0, st>>>(out, static_cast<const B*>(dout), static_cast<const B*>(q),
+                                         rows, order, n_chunks, T, hq, delta, dq,
+                                         static_cast<__half*>(q16), static_cast<__half*>(do16), err);
+  };
+  if (d == 128)
+    out_f32 ? go(preprocess_kernel<128, true>) : go(preprocess_kernel<128, false>);
+  else
+    out_f32 ? go(preprocess_kernel<64, true>) : go(preprocess_kernel<64, false>);
+  return cudaGetLastError() == cudaSuccess ? FCP_OK : FCP_ERR_CUDA;
+}
+
+}  // namespace fcp

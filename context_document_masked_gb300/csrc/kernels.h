@@ -1,0 +1,83 @@
+// Launch interfaces of the libfcp device kernels (internal to the library).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "../../include/fcp.h"
+
+namespace fcp {
+
+struct FwdParams {
+  const int32_t* pieces;   // plan piece table
+  const int32_t* segs;     // key segments
+  const int32_t* tiles;    // query tiles (piece, q_start, q_rows, cost)
+  const int32_t* order;    // tile indices to run, longest first
+  int32_t n_items;
+  int32_t kbuf_shift;      // subtracted from received-key rows (one-shard launches)
+  int32_t kv_lo, kv_hi;    // key block
+  int32_t T, hq, hkv;
+  float scale_log2;        // softmax scale * log2(e)
+  int32_t out_f32;
+  void* out;
+  float* lse;
+  int* err;
+  int64_t wait_ns;
+};
+
+struct FwdLaunch {
+  CUtensorMap tm_q, tm_k, tm_v, tm_kb, tm_vb;
+  FwdParams p;
+  int d;
+  int num_sms;
+};
+
+struct BwdParams {
+  const int32_t* pieces;
+  const int32_t* tiles;    // backward key tiles (piece, seg, key0, n, src, src_row, qt_first, n_qt)
+  const int32_t* order;
+  int32_t n_items;
+  int32_t kbuf_shift;
+  int32_t T, hq, hkv;
+  float scale;             // softmax scale
+  float scale_log2;
+  const float* lse;        // [Hq][T]
+  const float* delta;      // [Hq][T] rowsum(dO * O)
+  float* dq;               // [T][Hq][d] fp32, accumulated
+  float* dk;               // [T][Hkv][d] fp32, accumulated
+  float* dv;
+  int* err;
+  int64_t wait_ns;
+};
+
+struct BwdLaunch {
+  CUtensorMap tm_q, tm_do, tm_k, tm_v, tm_kb, tm_vb;
+  BwdParams p;
+  int d;
+  int num_sms;
+};
+
+int launch_attn_fwd(const FwdLaunch& a, cudaStream_t st);
+int launch_attn_bwd(const BwdLaunch& a, cudaStream_t st);
+
+// Row statistics D_i = <dO_i, O_i> for the rows of the given row chunks, dQ
+// rows set to zero, and fp16 copies of Q and dO for the backward's MMAs.
+int launch_bwd_preprocess(const void* out, bool out_f32, const void* dout, const void* q,
+                          const int32_t* rows,
+                          const int32_t* order, int32_t n_chunks, int32_t T, int32_t hq, int32_t d,
+                          float* delta, float* dq, void* q16, void* do16, int* err, cudaStream_t st);
+
+// fp16 copy of a bf16 array of n_elems (a multiple of 8) elements.
+int launch_convert_f16(const void* src, void* dst, int64_t n_elems, int* err, int num_sms,
+                       cudaStream_t st);
+
+// Gather of received KV rows: tasks (src_row, dst_row, nrows, shard).
+int launch_gather(const void* k, const void* v, const int32_t* tasks, int32_t n_tasks,
+                  int32_t dst_shift, int64_t row_bytes, void* kbuf, void* vbuf, int num_sms,
+                  cudaStream_t st);
+
+int launch_merge(const float* o_parts, const float* lse_parts, int32_t B, int64_t rows, int32_t hq,
+                 int32_t d, void* out, float* lse_out, int num_sms, cudaStream_t st);
+
+}  // namespace fcp

@@ -1,0 +1,186 @@
+// Device work tables of a plan.
+//
+// From each shard's pieces (query ranges) and key needs the planner derives
+// what the kernels iterate over:
+//   - key segments: the keys a piece needs, [doc start, piece end), cut into
+//     runs that the shard holds itself (read from K/V at their global rows)
+//     and runs received from other shards (read from the compacted
+//     kbuf/vbuf, in the order of the shard's kv_remote list);
+//   - forward query tiles of <= 128 rows, each inside one piece;
+//   - backward key tiles of <= 128 keys, each inside one segment;
+//   - gather runs (<= kCopyRows rows) and preprocess row chunks.
+// Tiles are listed longest first (by the number of tile pairs they cover) so
+// that a grid of one CTA per tile finishes the long rows early.
+#include <algorithm>
+#include <numeric>
+
+#include "plan.h"
+
+namespace fcp {
+
+namespace {
+
+struct Seg { int32_t src, src_row, key_start, len; };
+
+int64_t count_key_tiles(const std::vector<Seg>& segs, int32_t seg_begin, int32_t seg_count,
+                        int32_t q_last) {
+  int64_t n = 0;
+  for (int32_t s = seg_begin; s < seg_begin + seg_count; ++s) {
+    const Seg& g = segs[s];
+    if (g.key_start > q_last) break;
+    int64_t len = std::min<int64_t>(g.len, (int64_t)q_last - g.key_start + 1);
+    n += (len + kTileN - 1) / kTileN;
+  }
+  return n;
+}
+
+void append(std::vector<int32_t>& dev, int32_t* off, int32_t* cnt, int tb,
+            const std::vector<int32_t>& data, int32_t n_entries) {
+  while (dev.size() % 4) dev.push_back(0);  // 16-byte alignment of every table
+  off[tb] = (int32_t)dev.size();
+  cnt[tb] = n_entries;
+  dev.insert(dev.end(), data.begin(), data.end());
+}
+
+}  // namespace
+
+void Plan::build_work_tables() {
+  std::vector<int32_t> pieces, segs_flat, ftiles, btiles, copy, rows;
+  std::vector<Seg> segs;
+  std::vector<int32_t> fshard(N + 1, 0), bshard(N + 1, 0), cshard(N + 1, 0), rshard(N + 1, 0);
+  std::vector<int64_t> fcost, bcost;
+  int32_t piece_id = 0;
+  for (int32_t j = 0; j < N; ++j) {
+    const Shard& sh = shards[j];
+    fshard[j] = (int32_t)(ftiles.size() / 4);
+    bshard[j] = (int32_t)(btiles.size() / 8);
+    cshard[j] = (int32_t)(copy.size() / 4);
+    rshard[j] = (int32_t)(rows.size() / 2);
+    // Position of each remote range inside this shard's kbuf.
+    std::vector<int64_t> rpos(sh.kv_remote.size());
+    int64_t acc = sh.kbuf_base;
+    for (size_t r = 0; r < sh.kv_remote.size(); ++r) {
+      rpos[r] = acc;
+      const fcp_range& rr = sh.kv_remote[r];
+      for (int32_t a = rr.start; a < rr.end; a += kCopyRows) {
+        int32_t nr = std::min(kCopyRows, rr.end - a);
+        copy.insert(copy.end(), {a, (int32_t)(acc + (a - rr.start)), nr, j});
+      }
+      acc += rr.end - rr.start;
+    }
+    for (const Piece& p : sh.pieces) {
+      const int32_t ds = off[p.doc];
+      const int32_t seg_begin = (int32_t)segs.size();
+      // Walk [ds, p.end): own pieces of this doc and remote ranges of this doc
+      // are disjoint and together cover the needed range.
+      int32_t t = ds;
+      while (t < p.end) {
+        bool found = false;
+        for (const Piece& o : sh.pieces) {
+          if (o.doc == p.doc && o.start <= t && t < o.end) {
+            int32_t e = std::min(o.end, p.end);
+            segs.push_back(Seg{0, t, t, e - t});
+            t = e;
+            found = true;
+            break;
+          }
+        }
+        if (found) continue;
+        for (size_t r = 0; r < sh.kv_remote.size(); ++r) {
+          const fcp_range& rr = sh.kv_remote[r];
+          if (rr.doc == p.doc && rr.start <= t && t < rr.end) {
+            int32_t e = std::min(rr.end, p.end);
+            segs.push_back(Seg{1, (int32_t)(rpos[r] + (t - rr.start)), t, e - t});
+            t = e;
+            found = true;
+            break;
+          }
+        }
+        if (!found) break;  // unreachable for a consistent plan
+      }
+      const int32_t seg_count = (int32_t)segs.size() - seg_begin;
+      pieces.insert(pieces.end(), {j, p.doc, p.start, p.end, ds, seg_begin, seg_count, 0});
+      // Forward query tiles.
+      for (int32_t q0 = p.start; q0 < p.end; q0 += kTileM) {
+        int32_t qr = std::min(kTileM, p.end - q0);
+        int64_t c = count_key_tiles(segs, seg_begin, seg_count, q0 + qr - 1);
+        ftiles.insert(ftiles.end(), {piece_id, q0, qr, (int32_t)std::min<int64_t>(c, 1 << 30)});
+        fcost.push_back(c);
+      }
+      // Backward key tiles: every tile of every segment; the queries that see
+      // it are the piece's rows at or after the tile start.
+      for (int32_t s = seg_begin; s < seg_begin + seg_count; ++s) {
+        const Seg& g = segs[s];
+        for (int32_t k0 = 0; k0 < g.len; k0 += kTileN) {
+          int32_t kr = std::min(kTileN, g.len - k0);
+          int32_t key = g.key_start + k0;
+          int32_t qfirst = std::max(key, p.start);
+          int32_t qt_first = (qfirst - p.start) / kTileM;
+          int32_t n_qt = (p.end - p.start + kTileM - 1) / kTileM - qt_first;
+          btiles.insert(btiles.end(), {piece_id, s, key, kr, g.src, g.src_row + k0, qt_first, n_qt});
+          bcost.push_back(n_qt);
+        }
+      }
+      for (int32_t a = p.start; a < p.end; a += kRowChunk)
+        rows.insert(rows.end(), {a, std::min(kRowChunk, p.end - a)});
+      ++piece_id;
+    }
+  }
+  fshard[N] = (int32_t)(ftiles.size() / 4);
+  bshard[N] = (int32_t)(btiles.size() / 8);
+  cshard[N] = (int32_t)(copy.size() / 4);
+  rshard[N] = (int32_t)(rows.size() / 2);
+  // Longest-first orders. Within a shard the table itself is re-sorted too,
+  // so one-shard launches are longest-first as well.
+  auto sort_group = [](std::vector<int32_t>& tab, int width, std::vector<int64_t>& cost,
+                       const std::vector<int32_t>& shard_off, int N) {
+    std::vector<int32_t> out(tab.size());
+    std::vector<int64_t> cout(cost.size());
+    for (int j = 0; j < N; ++j) {
+      std::vector<int32_t> idx(shard_off[j + 1] - shard_off[j]);
+      std::iota(idx.begin(), idx.end(), shard_off[j]);
+      std::stable_sort(idx.begin(), idx.end(),
+                       [&](int32_t a, int32_t b) { return cost[a] > cost[b]; });
+      for (size_t i = 0; i < idx.size(); ++i) {
+        std::copy(tab.begin() + (size_t)idx[i] * width, tab.begin() + (size_t)(idx[i] + 1) * width,
+                  out.begin() + (size_t)(shard_off[j] + i) * width);
+        cout[shard_off[j] + i] = cost[idx[i]];
+      }
+    }
+    tab.swap(out);
+    cost.swap(cout);
+  };
+  sort_group(ftiles, 4, fcost, fshard, N);
+  sort_group(btiles, 8, bcost, bshard, N);
+  std::vector<int32_t> forder(fcost.size()), border(bcost.size());
+  std::iota(forder.begin(), forder.end(), 0);
+  std::iota(border.begin(), border.end(), 0);
+  std::stable_sort(forder.begin(), forder.end(), [&](int32_t a, int32_t b) { return fcost[a] > fcost[b]; });
+  std::stable_sort(border.begin(), border.end(), [&](int32_t a, int32_t b) { return bcost[a] > bcost[b]; });
+  size_t nid = std::max({forder.size(), border.size(), copy.size() / 4, rows.size() / 2, (size_t)1});
+  std::vector<int32_t> ident(nid);
+  std::iota(ident.begin(), ident.end(), 0);
+  std::vector<int32_t> kbase(N + 1);
+  for (int32_t j = 0; j < N; ++j) kbase[j] = (int32_t)shards[j].kbuf_base;
+  kbase[N] = (int32_t)total_remote;
+
+  for (const Seg& g : segs) segs_flat.insert(segs_flat.end(), {g.src, g.src_row, g.key_start, g.len});
+  dev.clear();
+  append(dev, tab_off, tab_cnt, TB_PIECES, pieces, (int32_t)(pieces.size() / 8));
+  append(dev, tab_off, tab_cnt, TB_SEGS, segs_flat, (int32_t)segs.size());
+  append(dev, tab_off, tab_cnt, TB_FTILES, ftiles, (int32_t)(ftiles.size() / 4));
+  append(dev, tab_off, tab_cnt, TB_FORDER, forder, (int32_t)forder.size());
+  append(dev, tab_off, tab_cnt, TB_FSHARD, fshard, N + 1);
+  append(dev, tab_off, tab_cnt, TB_BTILES, btiles, (int32_t)(btiles.size() / 8));
+  append(dev, tab_off, tab_cnt, TB_BORDER, border, (int32_t)border.size());
+  append(dev, tab_off, tab_cnt, TB_BSHARD, bshard, N + 1);
+  append(dev, tab_off, tab_cnt, TB_COPY, copy, (int32_t)(copy.size() / 4));
+  append(dev, tab_off, tab_cnt, TB_CSHARD, cshard, N + 1);
+  append(dev, tab_off, tab_cnt, TB_ROWS, rows, (int32_t)(rows.size() / 2));
+  append(dev, tab_off, tab_cnt, TB_RSHARD, rshard, N + 1);
+  append(dev, tab_off, tab_cnt, TB_IDENT, ident, (int32_t)ident.size());
+  append(dev, tab_off, tab_cnt, TB_KBASE, kbase, N + 1);
+  while ((dev.size() * 4) % 256) dev.push_back(0);
+}
+
+}  // namespace fcp

@@ -1,0 +1,269 @@
+"""Python binding of libfcp (include/fcp.h), argument marshalling only.
+
+Every computation runs in the C++ planner or the CUDA kernels of libfcp.so;
+PyTorch supplies device memory and streams. Importing this module loads the
+library and raises if it has not been built: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libfcp.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_INFEASIBLE, ERR_CAPACITY = range(7)
+POLICIES = {"llama3": 0, "perdoc": 1, "wholedoc": 2, "hybrid": 3}
+OUT_BF16, OUT_F32 = 0, 1
+
+EXPORTED = (
+    "fcp_strerror", "fcp_plan", "fcp_plan_free", "fcp_plan_shard", "fcp_plan_query_indices",
+    "fcp_plan_stats", "fcp_plan_per_doc_flags", "fcp_plan_device_bytes", "fcp_plan_upload",
+    "fcp_workspace_bytes", "fcp_gather_kv", "fcp_attn_fwd", "fcp_merge", "fcp_attn_bwd",
+    "fcp_get_device_status", "fcp_debug_set_wait_limit",
+)
+
+
+class FcpError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {_lib.fcp_strerror(status).decode()} (status {status})")
+
+
+class Range(C.Structure):
+    _fields_ = [("doc", C.c_int32), ("start", C.c_int32), ("end", C.c_int32)]
+
+
+class ShardView(C.Structure):
+    _fields_ = [
+        ("n_pieces", C.c_int32), ("pieces", C.POINTER(Range)),
+        ("n_need", C.c_int32), ("kv_need", C.POINTER(Range)),
+        ("n_remote", C.c_int32), ("kv_remote", C.POINTER(Range)),
+        ("tokens", C.c_int64), ("useful_pairs", C.c_int64), ("remote_rows", C.c_int64),
+        ("kbuf_base", C.c_int64),
+    ]
+
+
+class PlanStats(C.Structure):
+    _fields_ = [
+        ("cp", C.c_int32), ("n_docs", C.c_int32), ("T", C.c_int64), ("imbalance", C.c_double),
+        ("max_pairs", C.c_int64), ("total_pairs", C.c_int64), ("eq4_tokens", C.c_int64),
+        ("eq5_tokens", C.c_int64), ("remote_rows_total", C.c_int64), ("remote_rows_max", C.c_int64),
+        ("eq2_max_dev", C.c_int64), ("iterations", C.c_int32), ("n_per_doc", C.c_int32),
+    ]
+
+
+class DevPlan(C.Structure):
+    _fields_ = [
+        ("host", C.c_void_p), ("base", C.c_void_p), ("bytes", C.c_int64), ("n_shards", C.c_int32),
+        ("T", C.c_int32), ("total_remote_rows", C.c_int64), ("tables", C.c_int32 * 16),
+        ("counts", C.c_int32 * 16),
+    ]
+
+
+class Dims(C.Structure):
+    _fields_ = [("T", C.c_int32), ("hq", C.c_int32), ("hkv", C.c_int32), ("d", C.c_int32),
+                ("scale", C.c_float)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libfcp.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+    lib = C.CDLL(LIB_PATH)
+    vp, i32, i64, f64 = C.c_void_p, C.c_int32, C.c_int64, C.c_double
+    sig = {
+        "fcp_strerror": (C.c_char_p, [C.c_int]),
+        "fcp_plan": (C.c_int, [C.POINTER(C.c_int32), i32, i32, i32, f64, C.POINTER(vp)]),
+        "fcp_plan_free": (None, [vp]),
+        "fcp_plan_shard": (C.c_int, [vp, i32, C.POINTER(ShardView)]),
+        "fcp_plan_query_indices": (C.c_int, [vp, i32, C.POINTER(C.c_int32), i64, C.POINTER(i64)]),
+        "fcp_plan_stats": (C.c_int, [vp, C.POINTER(PlanStats)]),
+        "fcp_plan_per_doc_flags": (C.c_int, [vp, C.POINTER(C.c_int32), i32]),
+        "fcp_plan_device_bytes": (i64, [vp]),
+        "fcp_plan_upload": (C.c_int, [vp, vp, i64, vp, C.POINTER(DevPlan)]),
+        "fcp_workspace_bytes": (i64, [Dims, vp]),
+        "fcp_gather_kv": (C.c_int, [vp, vp, C.POINTER(DevPlan), i32, i32, i32, vp, vp, vp]),
+        "fcp_attn_fwd": (C.c_int, [vp, vp, vp, vp, vp, C.POINTER(DevPlan), i32, i32, i32, Dims, i32,
+                                   vp, vp, vp, i64, vp]),
+        "fcp_merge": (C.c_int, [vp, vp, i32, i64, i32, i32, vp, vp, vp]),
+        "fcp_attn_bwd": (C.c_int, [vp, vp, vp, vp, vp, vp, i32, vp, vp, C.POINTER(DevPlan), i32,
+                                   Dims, vp, vp, vp, vp, i64, vp]),
+        "fcp_get_device_status": (C.c_int, [vp, vp]),
+        "fcp_debug_set_wait_limit": (None, [i64]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+def _check(status: int, what: str):
+    if status != OK:
+        raise FcpError(status, what)
+
+
+def strerror(status: int) -> str:
+    return _lib.fcp_strerror(status).decode()
+
+
+# ---------------------------------------------------------------- plans
+
+
+class Plan:
+    """A host sharding plan (fcp_plan)."""
+
+    def __init__(self, doclens, cp: int, policy: str, target_imbalance: float = 1.05):
+        d = np.ascontiguousarray(np.asarray(doclens, dtype=np.int32))
+        self._ptr = C.c_void_p()
+        _check(_lib.fcp_plan(d.ctypes.data_as(C.POINTER(C.c_int32)), len(d), cp, POLICIES[policy],
+                             target_imbalance, C.byref(self._ptr)), "fcp_plan")
+        self.doclens = d
+        self.cp = cp
+        self.policy = policy
+
+    def __del__(self):
+        if getattr(self, "_ptr", None) and self._ptr.value:
+            _lib.fcp_plan_free(self._ptr)
+            self._ptr = C.c_void_p()
+
+    @property
+    def handle(self):
+        return self._ptr
+
+    def shard(self, j: int) -> dict:
+        v = ShardView()
+        _check(_lib.fcp_plan_shard(self._ptr, j, C.byref(v)), "fcp_plan_shard")
+
+        def rng(ptr, n):
+            return [(ptr[i].doc, ptr[i].start, ptr[i].end) for i in range(n)]
+        return {
+            "pieces": rng(v.pieces, v.n_pieces), "kv_need": rng(v.kv_need, v.n_need),
+            "kv_remote": rng(v.kv_remote, v.n_remote), "tokens": v.tokens,
+            "useful_pairs": v.useful_pairs, "remote_rows": v.remote_rows, "kbuf_base": v.kbuf_base,
+        }
+
+    def query_indices(self, j: int) -> np.ndarray:
+        n = C.c_int64()
+        st = _lib.fcp_plan_query_indices(self._ptr, j, None, 0, C.byref(n))
+        if st not in (OK, ERR_CAPACITY):
+            _check(st, "fcp_plan_query_indices")
+        out = np.empty(n.value, dtype=np.int32)
+        _check(_lib.fcp_plan_query_indices(self._ptr, j, out.ctypes.data_as(C.POINTER(C.c_int32)),
+                                           n.value, C.byref(n)), "fcp_plan_query_indices")
+        return out
+
+    def stats(self) -> dict:
+        s = PlanStats()
+        _check(_lib.fcp_plan_stats(self._ptr, C.byref(s)), "fcp_plan_stats")
+        return {f: getattr(s, f) for f, _ in PlanStats._fields_}
+
+    def per_doc_flags(self) -> list:
+        out = np.zeros(len(self.doclens), dtype=np.int32)
+        _check(_lib.fcp_plan_per_doc_flags(self._ptr, out.ctypes.data_as(C.POINTER(C.c_int32)),
+                                           len(out)), "fcp_plan_per_doc_flags")
+        return out.tolist()
+
+    def device_bytes(self) -> int:
+        return int(_lib.fcp_plan_device_bytes(self._ptr))
+
+    def upload(self, buf, stream=None) -> "DevicePlan":
+        """Copy the work tables into `buf` (a device tensor of >= device_bytes())."""
+        dp = DevPlan()
+        _check(_lib.fcp_plan_upload(self._ptr, C.c_void_p(buf.data_ptr()),
+                                    buf.numel() * buf.element_size(), _stream(stream), C.byref(dp)),
+               "fcp_plan_upload")
+        return DevicePlan(dp, self, buf)
+
+
+class DevicePlan:
+    """fcp_dev_plan plus references that keep the host plan and buffer alive."""
+
+    def __init__(self, dp: DevPlan, plan: Plan, buf):
+        self.c = dp
+        self.plan = plan
+        self.buf = buf
+
+    @property
+    def total_remote_rows(self) -> int:
+        return int(self.c.total_remote_rows)
+
+    def remote_rows(self, shard: int) -> int:
+        return self.total_remote_rows if shard < 0 else int(self.plan.shard(shard)["remote_rows"])
+
+
+# ---------------------------------------------------------------- device
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return C.c_void_p(stream)
+    return C.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return C.c_void_p(0 if t is None else t.data_ptr())
+
+
+def dims(T: int, hq: int, hkv: int, d: int, scale: float = 0.0) -> Dims:
+    return Dims(T, hq, hkv, d, scale)
+
+
+def workspace_bytes(dm: Dims, plan: "Plan | None" = None) -> int:
+    return int(_lib.fcp_workspace_bytes(dm, plan.handle if plan is not None else None))
+
+
+def gather_kv(k, v, dplan: DevicePlan, shard: int, kbuf, vbuf, stream=None):
+    _check(_lib.fcp_gather_kv(_ptr(k), _ptr(v), C.byref(dplan.c), shard, k.shape[1], k.shape[2],
+                              _ptr(kbuf), _ptr(vbuf), _stream(stream)), "fcp_gather_kv")
+
+
+def attn_fwd(q, k, v, kbuf, vbuf, dplan: DevicePlan, shard: int, out, lse, ws, kv_lo: int = 0,
+             kv_hi: int | None = None, scale: float = 0.0, stream=None):
+    import torch
+    T, hq, d = q.shape
+    dm = Dims(T, hq, k.shape[1], d, scale)
+    out_dtype = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
+    _check(_lib.fcp_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(kbuf), _ptr(vbuf), C.byref(dplan.c),
+                             shard, kv_lo, T if kv_hi is None else kv_hi, dm, out_dtype, _ptr(out),
+                             _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "fcp_attn_fwd")
+
+
+def merge(o_parts, lse_parts, out, lse_out, stream=None):
+    B, rows, hq, d = o_parts.shape
+    _check(_lib.fcp_merge(_ptr(o_parts), _ptr(lse_parts), B, rows, hq, d, _ptr(out), _ptr(lse_out),
+                          _stream(stream)), "fcp_merge")
+
+
+def attn_bwd(q, k, v, kbuf, vbuf, out, lse, dout, dplan: DevicePlan, shard: int, dq, dk, dv, ws,
+             scale: float = 0.0, stream=None):
+    import torch
+    T, hq, d = q.shape
+    dm = Dims(T, hq, k.shape[1], d, scale)
+    out_dtype = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
+    _check(_lib.fcp_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(kbuf), _ptr(vbuf), _ptr(out), out_dtype,
+                             _ptr(lse), _ptr(dout), C.byref(dplan.c), shard, dm, _ptr(dq), _ptr(dk),
+                             _ptr(dv), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "fcp_attn_bwd")
+
+
+def device_status(ws, stream=None) -> int:
+    return int(_lib.fcp_get_device_status(_ptr(ws), _stream(stream)))
+
+
+def debug_set_wait_limit(ns: int):
+    _lib.fcp_debug_set_wait_limit(ns)
+
+
+def raw_call(name: str, *args):
+    """Direct C-ABI call (for tests of argument validation)."""
+    return getattr(_lib, name)(*args)

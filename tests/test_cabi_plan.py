@@ -1,0 +1,103 @@
+"""The C-ABI library without a GPU: it loads, exports every function the
+header declares, and its C++ planner reproduces the oracle planner bit for bit
+(index lists exactly; the imbalance double identically)."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import synth
+from oracle import plan as P
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_exports_every_declared_function(lib):
+    header = open(os.path.join(ROOT, "include", "fcp.h")).read()
+    header = re.sub(r"/\*.*?\*/", "", header, flags=re.S)
+    declared = set(re.findall(r"\b(fcp_[a-z_0-9]+)\s*\(", header))
+    assert declared, "no declarations found"
+    import ctypes
+    so = ctypes.CDLL(lib.LIB_PATH)
+    for name in sorted(declared):
+        assert hasattr(so, name), name
+    assert declared == set(lib.EXPORTED)
+
+
+def _cases():
+    out = []
+    for cfg in (1, 2, 3, 4, 5):
+        D = synth.doc_lengths(cfg)
+        N = synth.WORKLOADS[cfg].cp
+        for pol in P.POLICIES:
+            out.append((f"cfg{cfg}-{pol}", D, N, pol, 1.05))
+    for seed in range(12):
+        for N in (1, 2, 3, 4, 8):
+            T = 2 * N * 40
+            D = synth.random_doc_lengths(T, seed=500 + seed)
+            for pol in P.POLICIES:
+                out.append((f"rand{seed}-N{N}-{pol}", D, N, pol, 1.0 + 0.05 * (seed % 4)))
+    return out
+
+
+CASES = _cases()
+
+
+@pytest.mark.parametrize("name,D,N,pol,R", CASES, ids=[c[0] for c in CASES])
+def test_cpp_planner_matches_oracle(lib, name, D, N, pol, R):
+    ref = P.make_plan(D, N, pol, R)
+    got = lib.Plan(D, N, pol, R)
+    st = got.stats()
+    assert st["imbalance"] == ref.imbalance          # same double, bit for bit
+    assert st["eq4_tokens"] == ref.eq4_tokens
+    assert st["eq5_tokens"] == ref.eq5_tokens
+    assert st["eq2_max_dev"] == ref.eq2_max_dev
+    assert st["iterations"] == ref.iterations
+    assert got.per_doc_flags() == ref.per_doc
+    for j in range(N):
+        s = got.shard(j)
+        r = ref.shards[j]
+        assert s["pieces"] == [(p.doc, p.start, p.end) for p in r.pieces]
+        assert s["kv_need"] == [tuple(x) for x in r.kv_need]
+        assert s["kv_remote"] == [tuple(x) for x in r.kv_remote]
+        assert s["tokens"] == r.tokens and s["useful_pairs"] == r.W
+        assert s["remote_rows"] == r.remote_rows
+        np.testing.assert_array_equal(got.query_indices(j), np.asarray(ref.query_indices(j), dtype=np.int32))
+
+
+def test_plan_errors(lib):
+    with pytest.raises(lib.FcpError) as e:
+        lib.Plan([5, 4], 2, "llama3")
+    assert e.value.status == lib.ERR_INFEASIBLE
+    with pytest.raises(lib.FcpError) as e:
+        lib.Plan([5, 4], 2, "wholedoc")
+    assert e.value.status == lib.ERR_INFEASIBLE
+    with pytest.raises(lib.FcpError) as e:
+        lib.Plan([5, 0, 3], 2, "perdoc")
+    assert e.value.status == lib.ERR_INVALID_ARG
+    with pytest.raises(lib.FcpError) as e:
+        lib.Plan([4, 4], 0, "perdoc")
+    assert e.value.status == lib.ERR_INVALID_ARG
+
+
+def test_device_calls_validate_before_launch(lib):
+    """Argument errors are reported synchronously; no GPU is touched."""
+    import ctypes
+    dm = lib.dims(64, 4, 2, 96)          # d = 96 unsupported
+    st = lib.raw_call("fcp_attn_fwd", None, None, None, None, None, None, -1, 0, 64, dm, 0,
+                      None, None, None, 0, None)
+    assert st == lib.ERR_INVALID_ARG      # null plan checked first
+    assert lib.raw_call("fcp_merge", None, None, 0, 10, 4, 128, None, None, None) == lib.ERR_INVALID_ARG
+    assert lib.raw_call("fcp_merge", None, None, 2, 10, 4, 96, None, None, None) == lib.ERR_UNSUPPORTED
+    assert lib.raw_call("fcp_get_device_status", None, None) == lib.ERR_INVALID_ARG
+    assert lib.workspace_bytes(lib.dims(1000, 8, 2, 128)) >= 256 + 8 * 1000 * 4 + 2 * 1000 * 8 * 128 * 2
+    assert lib.strerror(lib.ERR_TIMEOUT) == "bounded device wait expired"
+    del ctypes
+
+
+def test_work_tables_size(lib):
+    D = synth.doc_lengths(2)
+    p = lib.Plan(D, 4, "perdoc")
+    nbytes = p.device_bytes()
+    assert nbytes > 0 and nbytes % 256 == 0
