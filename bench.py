@@ -1,0 +1,403 @@
+"""Benchmark of the document-masked CP attention hot path on one GB300.
+
+One step = one pass of the whole path over one packed sequence with every CP
+shard in one launch: KV gather of the received prefix keys, forward, backward
+(preprocess + main kernel). The workload is the 32K packed sequence (lognormal
+document lengths, 32 query / 8 KV heads, d = 128, CP = 4, Per-Doc plan),
+synthetic and seeded. Every step's inputs (Q, K, V, dO: > 600 MB) exceed the
+129 MB L2, so no explicit flush is done between steps.
+
+Prints one JSON line. `--impl reference` times the fp64 CPU oracle instead, on
+a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+CFG = 2
+METRIC = "doc-masked attn useful TFLOPS fwd+bwd (% of GB300 BF16 peak); merge GB/s"
+UNIT = "TFLOP/s"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return {"hbm_gbs": m["hbm_gbs"], "bf16": m["bf16_tflops"], "bf16_sustained": m["bf16_tflops_sustained"],
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+def _workload():
+    w = synth.WORKLOADS[CFG]
+    D = synth.doc_lengths(CFG)
+    pairs = sum(L * (L + 1) // 2 for L in D)
+    return w, D, pairs
+
+
+def _config(w, D, extra=None):
+    c = {"workload": w.name, "tokens": w.T, "docs": len(D), "max_doc": max(D), "hq": w.Hq, "hkv": w.Hkv,
+         "d": w.d, "cp": w.cp, "policy": w.policy, "shards_per_launch": "all",
+         "l2": "inputs > L2 (Q,K,V,dO 0.67 GB), no flush"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples (every 50 ms) while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, index=0):
+        self.index = index
+        self.samples = []
+        self._p = None
+        self._t = None
+
+    def _read(self):
+        for line in self._p.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) == 7:
+                self.samples.append(parts)
+
+    def __enter__(self):
+        try:
+            self._p = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                        "--format=csv,noheader,nounits", "-lms", "50"],
+                                       stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+            time.sleep(0.3)   # first sample before the timed region starts
+        except OSError:
+            self._p = None
+        return self
+
+    def __exit__(self, *a):
+        if self._p is not None:
+            time.sleep(0.1)
+            self._p.terminate()
+            try:
+                self._p.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self._p.kill()
+            self._t.join(timeout=5)
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [v for v in (num(s[0]) for s in self.samples) if v is not None]
+        mx = [v for v in (num(s[1]) for s in self.samples) if v is not None]
+        pw = [v for v in (num(s[2]) for s in self.samples) if v is not None]
+        reasons = sorted({self.NAMES[i] for s in self.samples for i in range(4) if s[3 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None, "reasons": reasons, "samples": len(self.samples)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    return ws, rank
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    from context_document_masked_gb300 import fcp
+    from context_document_masked_gb300.session import CPAttention
+
+    world, rank = _dist()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    w, D, pairs = _workload()
+    T, hq, hkv, d = w.T, w.Hq, w.Hkv, w.d
+    seed = 1000 + CFG + rank          # independent replica per rank
+    q, k, v = synth.make_qkv(T, hq, hkv, d, seed=seed, device=dev)
+    do = synth.make_dout(T, hq, d, seed=seed, device=dev)
+    s = CPAttention(D, w.cp, w.policy, hq, hkv, d, device=dev)
+    out = torch.empty(T, hq, d, dtype=torch.float32, device=dev)
+    lse = torch.empty(hq, T, dtype=torch.float32, device=dev)
+    dq = torch.empty(T, hq, d, dtype=torch.float32, device=dev)
+    dk = torch.empty(T, hkv, d, dtype=torch.float32, device=dev)
+    dv = torch.empty_like(dk)
+    stream = torch.cuda.current_stream()
+
+    ev = {n: [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+          for n in ("gather", "fwd", "bwd", "end")}
+
+    def step(i=None):
+        if i is not None:
+            ev["gather"][i].record(stream)
+        s.gather(k, v)
+        if i is not None:
+            ev["fwd"][i].record(stream)
+        s.forward(q, k, v, out=out, lse=lse)
+        if i is not None:
+            ev["bwd"][i].record(stream)
+        s.backward(q, k, v, out, lse, do, dq=dq, dk=dk, dv=dv)
+        if i is not None:
+            ev["end"][i].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if s.device_status() != 0:
+        raise RuntimeError("device status reports a failed wait after warm-up")
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(i)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms_total = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    per = {n: statistics.mean(ev[a][i].elapsed_time(ev[b][i]) for i in range(args.steps))
+           for n, a, b in (("gather", "gather", "fwd"), ("fwd", "fwd", "bwd"), ("bwd", "bwd", "end"))}
+    fwd_flops = 4.0 * d * hq * pairs
+    bwd_flops = 10.0 * d * hq * pairs
+    value = world * (fwd_flops + bwd_flops) / (ms_step * 1e-3) / 1e12
+    pk = _peaks()
+    stats = s.stats()
+    remote_rows = stats["remote_rows_total"]
+    gather_bytes = 2 * 2 * remote_rows * hkv * d * 2
+
+    # Merge over the CP owners' key blocks (ring-style partials), same workload.
+    merge = _bench_merge(s, q, k, v, w, torch, fcp, pk)
+
+    # End to end through the public API: pinned host inputs -> device, plan,
+    # gather, forward, backward, results back to pinned host buffers.
+    e2e = _bench_e2e(args, D, w, seed, torch, CPAttention, fcp)
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    policies = {}
+    for pol in ("llama3", "perdoc", "wholedoc", "hybrid"):
+        try:
+            st = fcp.Plan(D, w.cp, pol).stats()
+            policies[pol] = {"imbalance": round(st["imbalance"], 4), "remote_rows": st["remote_rows_total"],
+                             "eq4_tokens": st["eq4_tokens"], "eq5_tokens": st["eq5_tokens"]}
+        except fcp.FcpError as e:
+            policies[pol] = {"error": str(e)}
+    cpu = _cpu_baseline(args.cpu_seconds)
+    peak = pk["bf16_sustained"]
+    bwd_ach = bwd_flops / (per["bwd"] * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 in, f16/bf16 MMA, f32 accumulate", "data": "synthetic",
+        "config": _config(w, D, {"parallelism": f"replicas{world}" if world > 1 else "single"}),
+        "pct_of_peak": round(100 * value / world / peak, 2),
+        "roofline": {"bound": "tensor", "kernel": "fcp_attn_bwd (preprocess + main)", "achieved": round(bwd_ach, 2),
+                     "peak": peak, "unit": "TFLOP/s", "frac": round(bwd_ach / peak, 4),
+                     "peak_note": f"{pk['source']} bf16 sustained; fp16 MMA has the same nominal rate",
+                     "traffic": None},
+        "kernels_ms": {k_: round(v_, 4) for k_, v_ in per.items()},
+        "fwd": {"tflops": round(fwd_flops / (per["fwd"] * 1e-3) / 1e12, 2),
+                "frac": round(fwd_flops / (per["fwd"] * 1e-3) / 1e12 / peak, 4)},
+        "bwd": {"tflops": round(bwd_ach, 2), "frac": round(bwd_ach / peak, 4)},
+        "gather": {"GB/s": round(gather_bytes / (per["gather"] * 1e-3) / 1e9, 1),
+                   "frac_hbm": round(gather_bytes / (per["gather"] * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+                   "bytes": gather_bytes, "remote_rows": remote_rows},
+        "merge": merge,
+        "useful_pairs": pairs,
+        "imbalance": policies,
+        "clocks": clk.summary(),
+        "gpu_launches": 6 * args.steps,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def _bench_merge(s, q, k, v, w, torch, fcp, pk):
+    """Forward over the CP owners' contiguous key blocks (fp32 partials), then
+    the merge kernel; GB/s on the algorithmic bytes of the merge."""
+    T, hq, d, B = w.T, w.Hq, w.d, w.cp
+    dev = q.device
+    o_parts = torch.empty(B, T, hq, d, dtype=torch.float32, device=dev)
+    l_parts = torch.empty(B, hq, T, dtype=torch.float32, device=dev)
+    bounds = [T * b // B for b in range(B + 1)]
+    for b in range(B):
+        s.forward(q, k, v, out=o_parts[b], lse=l_parts[b], kv_block=(bounds[b], bounds[b + 1]),
+                  out_dtype=torch.float32)
+    out = torch.empty(T, hq, d, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(hq, T, dtype=torch.float32, device=dev)
+    for _ in range(3):
+        fcp.merge(o_parts, l_parts, out, lse)
+    torch.cuda.synchronize()
+    n = 10
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n):
+        fcp.merge(o_parts, l_parts, out, lse)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    nonempty = int(torch.isfinite(l_parts).sum().item())
+    empty = B * hq * T - nonempty
+    rd = nonempty * (4 * d + 4) + empty * 4
+    wr = T * hq * (2 * d + 4)
+    dense = B * T * hq * (4 * d + 4) + wr
+    gbs = (rd + wr) / (ms * 1e-3) / 1e9
+    return {"GB/s": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 4), "frac_8TBs": round(gbs / 8000, 4),
+            "ms": round(ms, 4), "bytes": rd + wr, "dense_bytes": dense, "blocks": B,
+            "note": "parts with LSE=-inf are not read (no visible key in that block)"}
+
+
+def _bench_e2e(args, D, w, seed, torch, CPAttention, fcp):
+    T, hq, hkv, d = w.T, w.Hq, w.Hkv, w.d
+    q, k, v = synth.make_qkv(T, hq, hkv, d, seed=seed)
+    do = synth.make_dout(T, hq, d, seed=seed)
+    hq_, hk_, hv_, hdo = (x.pin_memory() for x in (q, k, v, do))
+    dev = torch.device("cuda", torch.cuda.current_device())
+    dq_h = torch.empty(T, hq, d, dtype=torch.float32).pin_memory()
+    dk_h = torch.empty(T, hkv, d, dtype=torch.float32).pin_memory()
+    dv_h = torch.empty_like(dk_h).pin_memory()
+    o_h = torch.empty(T, hq, d, dtype=torch.float32).pin_memory()
+    qd, kd, vd, dod = (torch.empty(x.shape, dtype=x.dtype, device=dev) for x in (q, k, v, do))
+    pairs = sum(L * (L + 1) // 2 for L in D)
+
+    def one():
+        for h, g in ((hq_, qd), (hk_, kd), (hv_, vd), (hdo, dod)):
+            g.copy_(h, non_blocking=True)
+        s = CPAttention(D, w.cp, w.policy, hq, hkv, d, device=dev)   # plan + upload + buffers
+        s.gather(kd, vd)
+        out, lse = s.forward(qd, kd, vd, out_dtype=torch.float32)
+        dq, dk, dv = s.backward(qd, kd, vd, out, lse, dod)
+        for g, h in ((out, o_h), (dq, dq_h), (dk, dk_h), (dv, dv_h)):
+            h.copy_(g, non_blocking=True)
+        torch.cuda.synchronize()
+
+    for _ in range(2):
+        one()
+    n = max(3, args.steps // 2)
+    t0 = time.perf_counter()
+    for _ in range(n):
+        one()
+    dt = (time.perf_counter() - t0) / n
+    h2d = sum(x.numel() * x.element_size() for x in (q, k, v, do))
+    d2h = sum(x.numel() * x.element_size() for x in (o_h, dq_h, dk_h, dv_h))
+    return {"value": round((14.0 * d * hq * pairs) / dt / 1e12, 2), "unit": UNIT, "ms_per_step": round(dt * 1e3, 3),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "includes": "H2D of Q,K,V,dO; plan build + upload + buffer allocation; gather; fwd; bwd; "
+                        "D2H of O (fp32), dQ, dK, dV"}
+
+
+def _cpu_baseline(seconds: float):
+    """The fp64 oracle (per-document form) on the host cores, on a bounded
+    sample of the workload: whole documents in order, one GQA group of heads,
+    until `seconds` have passed. Reported as useful TFLOP/s of the sample."""
+    from oracle import attention as A
+    w, D, _ = _workload()
+    G = w.Hq // w.Hkv
+    order = sorted(range(len(D)), key=lambda i: D[i])
+    t0 = time.perf_counter()
+    flops, done = 0.0, []
+    rng_seed = 4242
+    for i in order:
+        L = D[i]
+        q, k, v = synth.make_qkv(L, G, 1, w.d, seed=rng_seed + i)
+        do = synth.make_dout(L, G, w.d, seed=rng_seed + i)
+        cu = np.array([0, L])
+        o, lse = A.attention_per_doc(q, k, v, cu)
+        A.attention_bwd_per_doc(q, k, v, o, lse, do, cu)
+        flops += 14.0 * w.d * G * L * (L + 1) / 2
+        done.append(L)
+        if time.perf_counter() - t0 > seconds:
+            break
+    dt = time.perf_counter() - t0
+    try:
+        import threadpoolctl
+        blas = threadpoolctl.threadpool_info()
+        threads = max((b.get("num_threads", 0) for b in blas), default=None)
+    except ImportError:
+        threads = None
+    return {"value": round(flops / dt / 1e12, 6), "unit": UNIT, "cores": threads or os.cpu_count(),
+            "host_cpus": os.cpu_count(), "kind": "oracle", "seconds": round(dt, 2),
+            "sample": f"fp64 per-document fwd+bwd, {G} query heads (one GQA group), "
+                      f"{len(done)} whole documents (lengths {done}) of the workload"}
+
+
+def run_reference(args):
+    world, rank = _dist()
+    if rank != 0:
+        return
+    w, D, pairs = _workload()
+    vals = []
+    for _ in range(args.warmup):
+        _cpu_baseline(args.ref_seconds)
+    for _ in range(args.steps):
+        vals.append(_cpu_baseline(args.ref_seconds))
+    v = statistics.mean(x["value"] for x in vals)
+    step_s = statistics.mean(x["seconds"] for x in vals)
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": _config(w, D),
+            "cpu_baseline": {"value": round(v, 6), "unit": UNIT, "kind": "oracle", "cores": vals[0]["cores"],
+                             "sample": vals[0]["sample"]},
+            "e2e": {"value": round(v, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="fcp", choices=["fcp", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds", type=float, default=3.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "fcp":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()
