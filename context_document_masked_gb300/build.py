@@ -15,7 +15,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT_DIR, "libfcp.so")
-SOURCES = ["api.cu", "attn_fwd.cu", "attn_bwd.cu", "copy_kernels.cu", "plan.cpp", "tables.cpp"]
+SOURCES = ["api.cu", "attn_fwd.cu", "attn_bwd.cu", "copy_kernels.cu", "noalloc.cu", "plan.cpp",
+           "tables.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

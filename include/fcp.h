@@ -251,6 +251,40 @@ int fcp_attn_bwd(const void* q, const void* k, const void* v, const void* kbuf,
                  const void* dout, const fcp_dev_plan* plan, int32_t shard, fcp_dims dims,
                  float* dq, float* dk, float* dv, void* ws, int64_t ws_bytes, void* stream);
 
+/* Size of the device array that fcp_attn_fwd_noalloc uses as its scratch. */
+#define FCP_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/*
+ * fcp_attn_fwd_noalloc -- fcp_attn_fwd without a caller workspace and without
+ * any device allocation. The paper has no counterpart: this entry point exists
+ * for callers that cannot allocate device memory at call time -- for example a
+ * serving or training process that reserved all device memory up front (or
+ * handed it to another allocator) and forbids allocation on its request path,
+ * where a cudaMalloc would synchronise the device and can fail once memory is
+ * fragmented.
+ *   Arguments, layouts and results are those of fcp_attn_fwd, minus ws and
+ *   ws_bytes. The scratch (an error word and fp16 copies of V and of the
+ *   received V rows) is one file-scope device array of
+ *   FCP_NOALLOC_SCRATCH_BYTES bytes, held by every GPU that loads the library
+ *   until the process exits.
+ *   Limit: 256 + align256(T*Hkv*d*2) + align256(R*Hkv*d*2) bytes must fit in
+ *   that array, R = the received rows of this call (all shards' for shard ==
+ *   -1); larger inputs return FCP_ERR_CAPACITY before anything is launched.
+ *   The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any stream
+ *   capture. Nothing is allocated, by this library or through any allocating
+ *   library routine.
+ *   Every call shares the array and overwrites what the previous call left in
+ *   it (the error word is cleared at the start of each call): calls whose work
+ *   can overlap on the GPU -- on different streams without ordering -- race and
+ *   must not be issued. Device-side timeouts of this variant are recorded in
+ *   the shared array only; use fcp_attn_fwd with a workspace to read them.
+ */
+int fcp_attn_fwd_noalloc(const void* q, const void* k, const void* v, const void* kbuf,
+                         const void* vbuf, const fcp_dev_plan* plan, int32_t shard,
+                         int32_t kv_lo, int32_t kv_hi, fcp_dims dims, int32_t out_dtype,
+                         void* out, float* lse, void* stream);
+
 /*
  * fcp_get_device_status -- read the workspace error word (synchronizes the
  * stream). FCP_ERR_TIMEOUT if a bounded pipeline wait expired in a previous
