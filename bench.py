@@ -199,12 +199,13 @@ def run_gpu(args):
     remote_rows = stats["remote_rows_total"]
     gather_bytes = 2 * 2 * remote_rows * hkv * d * 2
 
+    legs = set(args.legs.split(","))
     # Merge over the CP owners' key blocks (ring-style partials), same workload.
-    merge = _bench_merge(s, q, k, v, w, torch, fcp, pk)
+    merge = _bench_merge(s, q, k, v, w, torch, fcp, pk) if "merge" in legs else None
 
     # End to end through the public API: pinned host inputs -> device, plan,
     # gather, forward, backward, results back to pinned host buffers.
-    e2e = _bench_e2e(args, D, w, seed, torch, CPAttention, fcp)
+    e2e = _bench_e2e(args, D, w, seed, torch, CPAttention, fcp) if "e2e" in legs else None
 
     if rank != 0:
         if world > 1:
@@ -218,7 +219,7 @@ def run_gpu(args):
                              "eq4_tokens": st["eq4_tokens"], "eq5_tokens": st["eq5_tokens"]}
         except fcp.FcpError as e:
             policies[pol] = {"error": str(e)}
-    cpu = _cpu_baseline(args.cpu_seconds)
+    cpu = _cpu_baseline(args.cpu_seconds) if "cpu" in legs else None
     peak = pk["bf16_sustained"]
     bwd_ach = bwd_flops / (per["bwd"] * 1e-3) / 1e12
     line = {
@@ -390,6 +391,8 @@ def main():
     ap.add_argument("--impl", default="fcp", choices=["fcp", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=3.0)
+    ap.add_argument("--legs", default="step,merge,e2e,cpu",
+                    help="parts to run: step (always), merge, e2e, cpu; e.g. 'step' for profiling")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "fcp":
         args.warmup = 3

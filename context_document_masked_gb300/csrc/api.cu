@@ -62,6 +62,20 @@ bool make_map(CUtensorMap* m, const void* ptr, int d, int heads, int64_t rows, b
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 [rows][heads][d] tensor, boxes of 32 x 1 x 128 with the 128-byte
+// swizzle: the target of the backward's dQ reduce-adds.
+bool make_map_f32(CUtensorMap* m, void* ptr, int d, int heads, int64_t rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)heads * d * 4};
+  cuuint32_t box[3] = {32, 1, 128};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 const int32_t* table(const fcp_dev_plan* dp, int tb) { return dp->base + dp->tables[tb]; }
@@ -366,7 +380,8 @@ int fcp_attn_bwd(const void* q, const void* k, const void* v, const void* kbuf, 
   std::memset(&a, 0, sizeof(a));
   bool ok = make_map(&a.tm_q, q16, dims.d, dims.hq, dims.T, true) &&
             make_map(&a.tm_do, do16, dims.d, dims.hq, dims.T, true) &&
-            make_map(&a.tm_k, k, dims.d, dims.hkv, dims.T) && make_map(&a.tm_v, v, dims.d, dims.hkv, dims.T);
+            make_map(&a.tm_k, k, dims.d, dims.hkv, dims.T) && make_map(&a.tm_v, v, dims.d, dims.hkv, dims.T) &&
+            make_map_f32(&a.tm_dq, dq, dims.d, dims.hq, dims.T);
   if (rrows > 0)
     ok = ok && make_map(&a.tm_kb, kbuf, dims.d, dims.hkv, rrows) &&
          make_map(&a.tm_vb, vbuf, dims.d, dims.hkv, rrows);

@@ -14,10 +14,11 @@
 //
 // Per step (one query head, one 128-row query tile), with keys as rows:
 //   S^T = K Q^T, dP^T = V dO^T                (TMEM)
-//   P^T = exp2(S^T scale log2e - LSE log2e)   (masked; bf16, back into TMEM)
-//   dS^T = P^T (dP^T - D)                     (bf16, shared memory)
+//   P^T = exp2(S^T scale log2e - LSE log2e)   (masked; fp16, back into TMEM)
+//   dS^T = P^T (dP^T - D)                     (fp16, shared memory)
 //   dV += P^T dO  (A operand from TMEM),  dK += dS^T Q,  dQ = dS K
-// and dQ is added to global memory with fp32 vector atomics.
+// and dQ leaves TMEM through shared memory with TMA bulk reduce-adds
+// (32-column chunks), one instruction per 16 KB.
 //
 // Tensor-core operands are fp16 (11 significant bits against bf16's 8): Q and
 // dO arrive as fp16 copies made by the preprocess pass, K and V tiles are
@@ -25,10 +26,18 @@
 // rounded to fp16. Every bf16 input inside the fp16 range converts exactly;
 // P <= 1 and |dS| stay far inside it.
 //
-// CTA roles (384 threads, persistent): warp 0 loads (TMA for K, V, Q, dO;
-// plain loads for LSE and D), warp 1 issues MMAs, warps 2-3 convert the K/V
-// tiles, warps 4-7 compute P and dS (one key row per thread) and write dK/dV,
-// warps 8-11 drain dQ (one query row per thread).
+// CTA roles (512 threads, persistent):
+//   warp 0       loads (TMA for K, V, Q, dO; plain loads for LSE and D)
+//   warp 1       issues MMAs and owns TMEM
+//   warps 2-3    convert each unit's K/V tiles to fp16
+//   warps 4-7    P and dS for query columns 0-63 (one key row per thread);
+//                dV to global at the end of a unit
+//   warps 8-11   P and dS for query columns 64-127; dK to global
+//   warps 12-15  dQ: TMEM -> shared memory -> TMA reduce-add into global
+// MMA order per step j, so that the exp work of step j+1 overlaps the dK/dQ
+// products of step j:  dV_j, S_{j+1}, dQ_j, dK_j, dP_{j+1}. Q tiles are
+// double-buffered; the dO tile is single-buffered (its last reader, dV_j,
+// runs first in the step).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -41,7 +50,7 @@ using namespace dev;
 
 namespace {
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 
 template <int D>
 struct BwdCfg {
@@ -50,12 +59,13 @@ struct BwdCfg {
   static constexpr int kK = 0;
   static constexpr int kV = kTile;
   static constexpr int kQ = 2 * kTile;           // 2 stages
-  static constexpr int kDO = 4 * kTile;          // 2 stages
-  static constexpr int kDS = 6 * kTile;          // 128 x 128 bf16
+  static constexpr int kDO = 4 * kTile;          // 1 stage
+  static constexpr int kStage = 5 * kTile;       // 2 x [128 rows][32 fp32] dQ chunks
+  static constexpr int kDS = kStage + 2 * 16384; // 128 x 128 fp16 (two 64-column panels)
   static constexpr int kStat = kDS + 128 * 128 * 2;  // [stage][lse2 | delta][128] fp32
   static constexpr int kSmem = kStat + 2 * 2 * 128 * 4;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColS = 0;           // S^T, then P^T (bf16) in its first 64 columns
+  static constexpr uint32_t kColS = 0;           // S^T; P^T (fp16) in cols [0,32) and [64,96)
   static constexpr uint32_t kColDP = 128;        // dP^T, then dQ
   static constexpr uint32_t kColDV = 256;
   static constexpr uint32_t kColDK = 256 + D;
@@ -82,9 +92,9 @@ __device__ __forceinline__ BwdItem decode(const BwdParams& p, int w) {
   return it;
 }
 
-// MMA with the A operand in TMEM (kind::f16, bf16 in, fp32 accumulate).
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
+// MMA with the A operand in TMEM (kind::f16, fp32 accumulate).
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
@@ -93,24 +103,54 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
-__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&v)[32]) {
-  float f[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
-  tmem_st32(taddr, f);
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
 }
 
+// TMA bulk reduce-add of a shared-memory tile into global memory.
+__device__ __forceinline__ void tma_reduce_add_3d(const void* tmap, const void* src, int c0, int c1,
+                                                  int c2) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
+      " [%0, {%2, %3, %4}], [%1];" ::"l"(reinterpret_cast<uint64_t>(tmap)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_le1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void drain_group_sync() {  // the 128 threads of the dQ warpgroup
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+// AND of `ok` over the 128 threads of the dQ warpgroup, so that its four warps
+// leave (or stay in) the loop together and never strand one at bar.sync.
+__device__ __forceinline__ bool drain_group_all(bool ok) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.and.pred po, 1, 128, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(out)
+      : "r"((uint32_t)ok)
+      : "memory");
+  return out != 0;
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_kb, const __grid_constant__ CUtensorMap tm_vb,
-                    const BwdParams p) {
+                    const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ __align__(8) uint64_t bar_kv_full, bar_kv_conv, bar_kv_empty, bar_drain;
-  __shared__ __align__(8) uint64_t bar_qdo_full[2], bar_qdo_empty[2];
+  __shared__ __align__(8) uint64_t bar_q_full[2], bar_q_empty[2], bar_do_full, bar_do_empty;
   __shared__ __align__(8) uint64_t bar_s_full, bar_dp_full, bar_p_ready, bar_ds_ready, bar_ds_free;
   __shared__ __align__(8) uint64_t bar_dq_full, bar_dq_free, bar_dkdv_full, bar_dkdv_free;
   __shared__ uint32_t tmem_base_sh;
@@ -127,18 +167,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bar_kv_empty, 1);
     mbar_init(&bar_drain, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&bar_qdo_full[s], 2);
-      mbar_init(&bar_qdo_empty[s], 1);
+      mbar_init(&bar_q_full[s], 2);
+      mbar_init(&bar_q_empty[s], 1);
     }
+    mbar_init(&bar_do_full, 1);
+    mbar_init(&bar_do_empty, 1);
     mbar_init(&bar_s_full, 1);
     mbar_init(&bar_dp_full, 1);
-    mbar_init(&bar_p_ready, 128);
-    mbar_init(&bar_ds_ready, 128);
+    mbar_init(&bar_p_ready, 256);
+    mbar_init(&bar_ds_ready, 256);
     mbar_init(&bar_ds_free, 1);
     mbar_init(&bar_dq_full, 1);
     mbar_init(&bar_dq_free, 128);
     mbar_init(&bar_dkdv_full, 1);
-    mbar_init(&bar_dkdv_free, 128);
+    mbar_init(&bar_dkdv_free, 256);
     abort_sh = 0;
     fence_barrier_init();
   }
@@ -153,6 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_v);
     prefetch_tmap(&tm_kb);
     prefetch_tmap(&tm_vb);
+    prefetch_tmap(&tm_dq);
   }
   tc_fence_before();
   __syncthreads();
@@ -165,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ loads
-    uint32_t kv_items = 0, qdo_cnt = 0;
+    uint32_t kv_items = 0, qc = 0, dc = 0;
     uint32_t issued_q[2] = {0, 0};
     bool ok = true;
     const float kLog2e = 1.4426950408889634f;
@@ -190,17 +233,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int h = it.g * G + j / it.n_qt;
         const int q0 = it.piece_start + (it.qt_first + j % it.n_qt) * 128;
         const int q_rows = min(128, it.piece_end - q0);
-        const int s = qdo_cnt & 1;
-        if (qdo_cnt >= 2) {
-          ok = mbar_wait(&bar_qdo_empty[s], ((qdo_cnt >> 1) - 1) & 1, wc);
+        // Q tile and the rows' LSE / D into Q stage s.
+        const int s = qc & 1;
+        if (qc >= 2) {
+          ok = mbar_wait(&bar_q_empty[s], ((qc >> 1) - 1) & 1, wc);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         }
         if (lane == 0) {
-          mbar_arrive_expect_tx(&bar_qdo_full[s], 2 * C::kTile);
-          for (int pn = 0; pn < C::kPanels; ++pn) {
-            tma_load_3d(smem + C::kQ + s * C::kTile + pn * 16384, &tm_q, &bar_qdo_full[s], pn * 64, h, q0);
-            tma_load_3d(smem + C::kDO + s * C::kTile + pn * 16384, &tm_do, &bar_qdo_full[s], pn * 64, h, q0);
-          }
+          mbar_arrive_expect_tx(&bar_q_full[s], C::kTile);
+          for (int pn = 0; pn < C::kPanels; ++pn)
+            tma_load_3d(smem + C::kQ + s * C::kTile + pn * 16384, &tm_q, &bar_q_full[s], pn * 64, h, q0);
           ++issued_q[s];
         }
         float* st = stat + s * 256;
@@ -212,14 +254,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           st[128 + r] = valid ? __ldg(p.delta + (size_t)h * p.T + q0 + r) : 0.f;
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_qdo_full[s]);
-        ++qdo_cnt;
+        if (lane == 0) mbar_arrive(&bar_q_full[s]);
+        ++qc;
+        // dO tile into the single dO buffer once dV of the previous step is done.
+        if (dc >= 1) {
+          ok = mbar_wait(&bar_do_empty, (dc - 1) & 1, wc);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bar_do_full, C::kTile);
+          for (int pn = 0; pn < C::kPanels; ++pn)
+            tma_load_3d(smem + C::kDO + pn * 16384, &tm_do, &bar_do_full, pn * 64, h, q0);
+        }
+        ++dc;
       }
     }
     if (lane == 0) {  // every copy this warp started has landed before the CTA exits
       if (kv_items) mbar_drain(&bar_kv_full, (kv_items - 1) & 1);
       for (int s = 0; s < 2; ++s)
-        if (issued_q[s]) mbar_drain(&bar_qdo_full[s], (issued_q[s] - 1) & 1);
+        if (issued_q[s]) mbar_drain(&bar_q_full[s], (issued_q[s] - 1) & 1);
+      if (dc) mbar_drain(&bar_do_full, (dc - 1) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -228,62 +282,86 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_kd = idesc_f16kind(128, D, false, true, false);     // dV, dK
       constexpr uint32_t id_dq = idesc_f16kind(128, D, true, true, false);      // dQ = dS K
       const uint32_t sK = smem_u32(smem + C::kK), sV = smem_u32(smem + C::kV);
-      const uint32_t sDS = smem_u32(smem + C::kDS);
-      uint32_t kv_items = 0, qdo_cnt = 0, gstep = 0, items = 0;
+      const uint32_t sDO = smem_u32(smem + C::kDO), sDS = smem_u32(smem + C::kDS);
+      uint32_t kv_items = 0, qc = 0, dc = 0, gstep = 0, items = 0;
       bool ok = true;
+      auto qaddr = [&](uint32_t c) { return smem_u32(smem + C::kQ + (c & 1) * C::kTile); };
+      auto issue_s = [&](uint32_t c) {
+        const uint32_t sQ = qaddr(c);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_bf16_ss(tmem + C::kColS, smem_desc_sw128(sK + off, 0, 1024),
+                      smem_desc_sw128(sQ + off, 0, 1024), id_sq, kk > 0);
+        }
+        mma_commit(&bar_s_full);
+      };
+      auto issue_dp = [&]() {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_bf16_ss(tmem + C::kColDP, smem_desc_sw128(sV + off, 0, 1024),
+                      smem_desc_sw128(sDO + off, 0, 1024), id_sq, kk > 0);
+        }
+        mma_commit(&bar_dp_full);
+      };
       for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
         const BwdItem it = decode(p, w);
         const int nsteps = G * it.n_qt;
         if (!(ok = mbar_wait(&bar_kv_conv, kv_items & 1, wc))) break;
+        tc_fence_after();
+        // Prologue of the unit: S_0 and dP_0.
+        if (!(ok = mbar_wait(&bar_q_full[qc & 1], (qc >> 1) & 1, wc))) break;
+        tc_fence_after();
+        issue_s(qc);
+        if (gstep > 0 && !(ok = mbar_wait(&bar_dq_free, (gstep - 1) & 1, wc))) break;
+        if (!(ok = mbar_wait(&bar_do_full, dc & 1, wc))) break;
+        tc_fence_after();
+        issue_dp();
         for (int j = 0; j < nsteps; ++j, ++gstep) {
-          const uint32_t c = qdo_cnt + j, s = c & 1;
-          const uint32_t sQ = smem_u32(smem + C::kQ + s * C::kTile);
-          const uint32_t sDO = smem_u32(smem + C::kDO + s * C::kTile);
-          if (!(ok = mbar_wait(&bar_qdo_full[s], (c >> 1) & 1, wc))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_bf16_ss(tmem + C::kColS, smem_desc_sw128(sK + off, 0, 1024),
-                        smem_desc_sw128(sQ + off, 0, 1024), id_sq, kk > 0);
-          }
-          mma_commit(&bar_s_full);
-          if (gstep > 0 && !(ok = mbar_wait(&bar_dq_free, (gstep - 1) & 1, wc))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_bf16_ss(tmem + C::kColDP, smem_desc_sw128(sV + off, 0, 1024),
-                        smem_desc_sw128(sDO + off, 0, 1024), id_sq, kk > 0);
-          }
-          mma_commit(&bar_dp_full);
+          const uint32_t c = qc + j;
+          const uint32_t sQ = qaddr(c);
           if (!(ok = mbar_wait(&bar_p_ready, gstep & 1, wc))) break;
           if (j == 0 && items > 0 && !(ok = mbar_wait(&bar_dkdv_free, (items - 1) & 1, wc))) break;
           tc_fence_after();
+          // dV += P^T dO, P^T from TMEM: q columns 0-63 in cols [0,32), 64-127 in [64,96).
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ts(tmem + C::kColDV, tmem + C::kColS + kk * 8,
-                        smem_desc_sw128(sDO + kk * 2048, 16384, 1024), id_kd, (j > 0 || kk > 0));
+            mma_f16_ts(tmem + C::kColDV, tmem + C::kColS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
+                       smem_desc_sw128(sDO + kk * 2048, 16384, 1024), id_kd, (j > 0 || kk > 0));
+          mma_commit(&bar_do_empty);
+          if (j + 1 < nsteps) {  // S region is free once dV (issued above) has read P^T
+            if (!(ok = mbar_wait(&bar_q_full[(c + 1) & 1], ((c + 1) >> 1) & 1, wc))) break;
+            tc_fence_after();
+            issue_s(c + 1);
+          }
           if (!(ok = mbar_wait(&bar_ds_ready, gstep & 1, wc))) break;
           tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ss(tmem + C::kColDP, smem_desc_sw128(sDS + kk * 2048, 16384, 1024),
+                        smem_desc_sw128(sK + kk * 2048, 16384, 1024), id_dq, kk > 0);
+          mma_commit(&bar_dq_full);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
             mma_bf16_ss(tmem + C::kColDK, smem_desc_sw128(sDS + aoff, 0, 1024),
                         smem_desc_sw128(sQ + kk * 2048, 16384, 1024), id_kd, (j > 0 || kk > 0));
           }
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ss(tmem + C::kColDP, smem_desc_sw128(sDS + kk * 2048, 16384, 1024),
-                        smem_desc_sw128(sK + kk * 2048, 16384, 1024), id_dq, kk > 0);
-          mma_commit(&bar_dq_full);
           mma_commit(&bar_ds_free);
-          mma_commit(&bar_qdo_empty[s]);
+          mma_commit(&bar_q_empty[c & 1]);
+          if (j + 1 < nsteps) {  // DP region is free once dQ_j has been read out
+            if (!(ok = mbar_wait(&bar_dq_free, gstep & 1, wc))) break;
+            if (!(ok = mbar_wait(&bar_do_full, (dc + j + 1) & 1, wc))) break;
+            tc_fence_after();
+            issue_dp();
+          }
         }
         if (!ok) break;
         mma_commit(&bar_dkdv_full);
         mma_commit(&bar_kv_empty);
-        qdo_cnt += nsteps;
+        qc += nsteps;
+        dc += nsteps;
         ++kv_items;
         ++items;
       }
@@ -314,12 +392,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++items;
     }
     if (ovf) atomicOr(p.err, 4);
-  } else if (warp >= 4 && warp < 8) {
+  } else if (warp < 12) {
     // ------------------------------------------------------------ P and dS
-    const int kr = tid - 128;
+    const int half = (warp - 4) >> 2;       // query columns [64*half, 64*half + 64)
+    const int kr = (warp & 3) * 32 + lane;  // key row == TMEM lane
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    const uint32_t ds_row = smem_u32(smem + C::kDS);
-    uint32_t qdo_cnt = 0, gstep = 0, items = 0;
+    const uint32_t s_cols = lane_base + C::kColS + 64 * half;
+    const uint32_t dp_cols = lane_base + C::kColDP + 64 * half;
+    const uint32_t ds_panel = smem_u32(smem + C::kDS) + half * 16384;
+    uint32_t qc = 0, gstep = 0, items = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
       const BwdItem it = decode(p, w);
@@ -327,18 +408,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool key_valid = kr < it.n;
       const int key = it.key0 + kr;
       for (int j = 0; j < nsteps; ++j, ++gstep) {
-        const uint32_t c = qdo_cnt + j, s = c & 1;
+        const uint32_t c = qc + j, s = c & 1;
         const int q0 = it.piece_start + (it.qt_first + j % it.n_qt) * 128;
-        const int lim = key - q0;  // query columns below lim cannot see this key
-        ok = mbar_wait(&bar_s_full, gstep & 1, wc) && mbar_wait(&bar_qdo_full[s], (c >> 1) & 1, wc);
+        const int lim = key - q0 - 64 * half;  // local columns below lim cannot see this key
+        ok = mbar_wait(&bar_s_full, gstep & 1, wc) && mbar_wait(&bar_q_full[s], (c >> 1) & 1, wc);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
-        const float* st = stat + s * 256;
-        uint32_t pk[64];
+        const float* st = stat + s * 256 + 64 * half;
+        uint32_t pk[32];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < 2; ++cc) {
           float v[32];
-          tmem_ld32(lane_base + C::kColS + cc * 32, v);
+          tmem_ld32(s_cols + cc * 32, v);
           tmem_ld_wait();
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
@@ -351,14 +432,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         {
-          uint32_t a[32], b[32];
+          float f[32];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            a[e] = pk[e];
-            b[e] = pk[32 + e];
-          }
-          tmem_st32u(lane_base + C::kColS, a);
-          tmem_st32u(lane_base + C::kColS + 32, b);
+          for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(pk[e]);
+          tmem_st32(s_cols, f);  // P^T over the S values just read (same rows, own columns)
           tmem_st_wait();
         }
         tc_fence_before();
@@ -368,64 +445,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < 2; ++cc) {
           float v[32];
-          tmem_ld32(lane_base + C::kColDP + cc * 32, v);
+          tmem_ld32(dp_cols + cc * 32, v);
           tmem_ld_wait();
           uint32_t o[16];
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             const int col = cc * 32 + e;
             const uint32_t pp = pk[col >> 1];
-            const float d0 = f16_lo(pp) * (v[e] - st[128 + col]);
-            const float d1 = f16_hi(pp) * (v[e + 1] - st[128 + col + 1]);
-            o[e >> 1] = pack_f16(d0, d1);
+            o[e >> 1] = pack_f16(f16_lo(pp) * (v[e] - st[128 + col]),
+                                 f16_hi(pp) * (v[e + 1] - st[128 + col + 1]));
           }
-          // 32 query columns = 4 swizzle chunks of 8 in panel cc/2.
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const int chunk = (cc & 1) * 4 + q4;
-            st_shared_v4(ds_row + (cc >> 1) * 16384 + sw128_offset(kr, chunk), o[4 * q4],
-                         o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
-          }
+          for (int q4 = 0; q4 < 4; ++q4)
+            st_shared_v4(ds_panel + sw128_offset(kr, cc * 4 + q4), o[4 * q4], o[4 * q4 + 1],
+                         o[4 * q4 + 2], o[4 * q4 + 3]);
         }
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&bar_ds_ready);
       }
       if (!ok) break;
-      qdo_cnt += nsteps;
-      // dK, dV of this key tile -> global rows (scatter-add over shards and pieces).
+      qc += nsteps;
+      // dV (columns-0 group) or dK (columns-64 group) of this key tile -> global rows.
       ok = mbar_wait(&bar_dkdv_full, items & 1, wc);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
       const size_t gbase = ((size_t)key * p.hkv + it.g) * D;
+      float* dst = (half == 0 ? p.dv : p.dk) + gbase;
+      const uint32_t src_col = lane_base + (half == 0 ? C::kColDV : C::kColDK);
+      const float mul = half == 0 ? 1.f : p.scale;
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
-        float v[32], k2[32];
-        tmem_ld32(lane_base + C::kColDV + cc * 32, v);
-        tmem_ld32(lane_base + C::kColDK + cc * 32, k2);
+        float v[32];
+        tmem_ld32(src_col + cc * 32, v);
         tmem_ld_wait();
         if (key_valid) {
-          float4* dvp = reinterpret_cast<float4*>(p.dv + gbase + cc * 32);
-          float4* dkp = reinterpret_cast<float4*>(p.dk + gbase + cc * 32);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            atomicAdd(dvp + e, make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]));
-            atomicAdd(dkp + e, make_float4(k2[4 * e] * p.scale, k2[4 * e + 1] * p.scale,
-                                           k2[4 * e + 2] * p.scale, k2[4 * e + 3] * p.scale));
-          }
+          for (int e = 0; e < 8; ++e)
+            red_add_v4(dst + cc * 32 + 4 * e, v[4 * e] * mul, v[4 * e + 1] * mul, v[4 * e + 2] * mul,
+                       v[4 * e + 3] * mul);
         }
       }
       tc_fence_before();
       mbar_arrive(&bar_dkdv_free);
       ++items;
     }
-  } else if (warp >= 8) {
+  } else {
     // ------------------------------------------------------------ dQ drain
-    const int r = tid - 256;
+    // Thread r holds query row q0 + r. Each 32-column chunk goes to one of two
+    // shared-memory staging tiles (the 128-byte swizzled layout of a
+    // [128 rows][32 fp32] TMA box) and one thread reduce-adds it into dQ.
+    // Rows past the piece end hold exact zeros (their P and dS are zero).
+    const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    uint32_t gstep = 0;
+    uint8_t* stage = smem + C::kStage;
+    uint32_t gstep = 0, chunks = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
       const BwdItem it = decode(p, w);
@@ -433,27 +509,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < nsteps; ++j, ++gstep) {
         const int h = it.g * G + j / it.n_qt;
         const int q0 = it.piece_start + (it.qt_first + j % it.n_qt) * 128;
-        const bool row_valid = r < min(128, it.piece_end - q0);
-        ok = mbar_wait(&bar_dq_full, gstep & 1, wc);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        ok = drain_group_all(mbar_wait(&bar_dq_full, gstep & 1, wc));
+        if (!ok) break;
         tc_fence_after();
-        float4* dst = reinterpret_cast<float4*>(p.dq + ((size_t)(q0 + r) * p.hq + h) * D);
 #pragma unroll 1
-        for (int cc = 0; cc < D / 32; ++cc) {
+        for (int cc = 0; cc < D / 32; ++cc, ++chunks) {
           float v[32];
           tmem_ld32(lane_base + C::kColDP + cc * 32, v);
           tmem_ld_wait();
-          if (row_valid) {
+          if (cc == D / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(&bar_dq_free);  // every dQ column of this step is in registers
+          }
+          uint8_t* buf = stage + (chunks & 1) * 16384;
+          if (r == 0) bulk_wait_read_le1();  // the reduce that last read `buf` is done with it
+          drain_group_sync();
+          const uint32_t row = smem_u32(buf);
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              atomicAdd(dst + cc * 8 + e, make_float4(v[4 * e] * p.scale, v[4 * e + 1] * p.scale,
-                                                      v[4 * e + 2] * p.scale, v[4 * e + 3] * p.scale));
+          for (int q4 = 0; q4 < 8; ++q4)
+            st_shared_v4(row + sw128_offset(r, q4), __float_as_uint(v[4 * q4] * p.scale),
+                         __float_as_uint(v[4 * q4 + 1] * p.scale), __float_as_uint(v[4 * q4 + 2] * p.scale),
+                         __float_as_uint(v[4 * q4 + 3] * p.scale));
+          fence_proxy_async_smem();
+          drain_group_sync();
+          if (r == 0) {
+            tma_reduce_add_3d(&tm_dq, buf, cc * 32, h, q0);
+            bulk_commit();
           }
         }
-        tc_fence_before();
-        mbar_arrive(&bar_dq_free);
       }
     }
+    if (r == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -482,7 +568,7 @@ static int launch_bwd_impl(const BwdLaunch& a, cudaStream_t st) {
   if (n_work == 0) return FCP_OK;
   const int grid = n_work < a.num_sms ? n_work : a.num_sms;
   attn_bwd_kernel<D><<<grid, kThreads, C::kSmem, st>>>(a.tm_q, a.tm_do, a.tm_k, a.tm_v, a.tm_kb,
-                                                      a.tm_vb, a.p);
+                                                      a.tm_vb, a.tm_dq, a.p);
   return cudaGetLastError() == cudaSuccess ? FCP_OK : FCP_ERR_CUDA;
 }
 

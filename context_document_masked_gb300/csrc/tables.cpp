@@ -9,8 +9,10 @@
 //   - forward query tiles of <= 128 rows, each inside one piece;
 //   - backward key tiles of <= 128 keys, each inside one segment;
 //   - gather runs (<= kCopyRows rows) and preprocess row chunks.
-// Tiles are listed longest first (by the number of tile pairs they cover) so
-// that a grid of one CTA per tile finishes the long rows early.
+// Tiles are listed piece by piece (pieces ordered by their longest tile) and,
+// inside a piece, longest first (by the number of tile pairs they cover): the
+// CTAs running at the same time then share one piece's query rows and keys
+// in L2, and the long rows start early.
 #include <algorithm>
 #include <numeric>
 
@@ -49,6 +51,7 @@ void Plan::build_work_tables() {
   std::vector<Seg> segs;
   std::vector<int32_t> fshard(N + 1, 0), bshard(N + 1, 0), cshard(N + 1, 0), rshard(N + 1, 0);
   std::vector<int64_t> fcost, bcost;
+  std::vector<int32_t> fpiece, bpiece;
   int32_t piece_id = 0;
   for (int32_t j = 0; j < N; ++j) {
     const Shard& sh = shards[j];
@@ -106,6 +109,7 @@ void Plan::build_work_tables() {
         int64_t c = count_key_tiles(segs, seg_begin, seg_count, q0 + qr - 1);
         ftiles.insert(ftiles.end(), {piece_id, q0, qr, (int32_t)std::min<int64_t>(c, 1 << 30)});
         fcost.push_back(c);
+        fpiece.push_back(piece_id);
       }
       // Backward key tiles: every tile of every segment; the queries that see
       // it are the piece's rows at or after the tile start.
@@ -119,6 +123,7 @@ void Plan::build_work_tables() {
           int32_t n_qt = (p.end - p.start + kTileM - 1) / kTileM - qt_first;
           btiles.insert(btiles.end(), {piece_id, s, key, kr, g.src, g.src_row + k0, qt_first, n_qt});
           bcost.push_back(n_qt);
+          bpiece.push_back(piece_id);
         }
       }
       for (int32_t a = p.start; a < p.end; a += kRowChunk)
@@ -130,33 +135,55 @@ void Plan::build_work_tables() {
   bshard[N] = (int32_t)(btiles.size() / 8);
   cshard[N] = (int32_t)(copy.size() / 4);
   rshard[N] = (int32_t)(rows.size() / 2);
-  // Longest-first orders. Within a shard the table itself is re-sorted too,
-  // so one-shard launches are longest-first as well.
+  // Piece-major, longest-first orders. A piece's rank is the position of its
+  // longest tile among all pieces' longest tiles.
+  auto ranks = [&](const std::vector<int64_t>& cost, const std::vector<int32_t>& piece) {
+    const int32_t np = piece_id;
+    std::vector<int64_t> pmax(np, -1);
+    for (size_t i = 0; i < cost.size(); ++i) pmax[piece[i]] = std::max(pmax[piece[i]], cost[i]);
+    std::vector<int32_t> idx(np), rank(np);
+    std::iota(idx.begin(), idx.end(), 0);
+    std::stable_sort(idx.begin(), idx.end(), [&](int32_t a, int32_t b) { return pmax[a] > pmax[b]; });
+    for (int32_t r = 0; r < np; ++r) rank[idx[r]] = r;
+    return rank;
+  };
+  const std::vector<int32_t> frank = ranks(fcost, fpiece), brank = ranks(bcost, bpiece);
   auto sort_group = [](std::vector<int32_t>& tab, int width, std::vector<int64_t>& cost,
+                       std::vector<int32_t>& piece, const std::vector<int32_t>& rank,
                        const std::vector<int32_t>& shard_off, int N) {
-    std::vector<int32_t> out(tab.size());
+    std::vector<int32_t> out(tab.size()), pout(piece.size());
     std::vector<int64_t> cout(cost.size());
     for (int j = 0; j < N; ++j) {
       std::vector<int32_t> idx(shard_off[j + 1] - shard_off[j]);
       std::iota(idx.begin(), idx.end(), shard_off[j]);
-      std::stable_sort(idx.begin(), idx.end(),
-                       [&](int32_t a, int32_t b) { return cost[a] > cost[b]; });
+      std::stable_sort(idx.begin(), idx.end(), [&](int32_t a, int32_t b) {
+        if (rank[piece[a]] != rank[piece[b]]) return rank[piece[a]] < rank[piece[b]];
+        return cost[a] > cost[b];
+      });
       for (size_t i = 0; i < idx.size(); ++i) {
         std::copy(tab.begin() + (size_t)idx[i] * width, tab.begin() + (size_t)(idx[i] + 1) * width,
                   out.begin() + (size_t)(shard_off[j] + i) * width);
         cout[shard_off[j] + i] = cost[idx[i]];
+        pout[shard_off[j] + i] = piece[idx[i]];
       }
     }
     tab.swap(out);
     cost.swap(cout);
+    piece.swap(pout);
   };
-  sort_group(ftiles, 4, fcost, fshard, N);
-  sort_group(btiles, 8, bcost, bshard, N);
+  sort_group(ftiles, 4, fcost, fpiece, frank, fshard, N);
+  sort_group(btiles, 8, bcost, bpiece, brank, bshard, N);
   std::vector<int32_t> forder(fcost.size()), border(bcost.size());
   std::iota(forder.begin(), forder.end(), 0);
   std::iota(border.begin(), border.end(), 0);
-  std::stable_sort(forder.begin(), forder.end(), [&](int32_t a, int32_t b) { return fcost[a] > fcost[b]; });
-  std::stable_sort(border.begin(), border.end(), [&](int32_t a, int32_t b) { return bcost[a] > bcost[b]; });
+  std::stable_sort(forder.begin(), forder.end(), [&](int32_t a, int32_t b) {
+    if (frank[fpiece[a]] != frank[fpiece[b]]) return frank[fpiece[a]] < frank[fpiece[b]];
+    return fcost[a] > fcost[b];
+  });
+  std::stable_sort(border.begin(), border.end(), [&](int32_t a, int32_t b) {
+    if (brank[bpiece[a]] != brank[bpiece[b]]) return brank[bpiece[a]] < brank[bpiece[b]];
+    return bcost[a] > bcost[b];
+  });
   size_t nid = std::max({forder.size(), border.size(), copy.size() / 4, rows.size() / 2, (size_t)1});
   std::vector<int32_t> ident(nid);
   std::iota(ident.begin(), ident.end(), 0);
