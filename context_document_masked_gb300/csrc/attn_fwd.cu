@@ -24,11 +24,15 @@
 //               tcgen05.mma, accumulators in TMEM; allocates TMEM.
 //   warps 4-7   softmax for head 0 of the pair, warps 8-11 for head 1: read
 //               S from TMEM (one row per thread), mask, update the running
-//               max / sum, write P (fp16) to shared memory, rescale O in TMEM
-//               when the max grows by more than 2^8, and finish the rows.
+//               max / sum, write P (fp16) back into TMEM over S, rescale O in
+//               TMEM when the max grows by more than 2^8, and finish the rows.
+// P V takes P straight from TMEM (the A operand) and V from shared memory.
 // Q K^T runs on the bf16 inputs; P V runs on fp16 operands (P <= 2^8 after
 // the lazy rescale, V from an fp16 copy), whose 11 significant bits keep the
-// rounding of P four times below bf16's.
+// rounding of P four times below bf16's. The MMAs of one thread run in issue
+// order, so S_i(t+1), issued after P_i(t) V, lands only after that product
+// has read P_i(t) and updated O_i: its completion also tells the softmax
+// group that O_i may be rescaled.
 // The two heads ping-pong: while one softmax group works on its S, the
 // tensor core runs the other head's P*V and next S.
 #include <cuda.h>
@@ -48,17 +52,15 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max
 
 template <int D>
 struct FwdCfg {
-  static constexpr int kStages = D == 128 ? 3 : 6;
+  static constexpr int kStages = D == 128 ? 5 : 8;
   static constexpr int kPanels = D / 64;                 // 64-column swizzle panels per row
   static constexpr int kTileBytes = 128 * D * 2;         // one Q/K/V tile
-  static constexpr int kPBytes = 128 * 128 * 2;
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = 2 * kTileBytes;
-  static constexpr int kPOff = kKVOff + kStages * kTileBytes;
-  static constexpr int kSmem = kPOff + 2 * kPBytes;
+  static constexpr int kSmem = kKVOff + kStages * kTileBytes;
   static constexpr int kSmemAlloc = kSmem + 1024;        // slack for 1024-byte alignment
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColS = 0;                   // S_i at i*128
+  static constexpr uint32_t kColS = 0;                   // S_i at i*128; P_i (fp16) over its first 64
   static constexpr uint32_t kColO = 256;                 // O_i at 256 + i*D
 };
 
@@ -194,7 +196,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   uint8_t* sQ = smem + C::kQOff;
   uint8_t* sKV = smem + C::kKVOff;
-  uint8_t* sP = smem + C::kPOff;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -249,7 +250,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       const uint32_t q_base = smem_u32(sQ);
       const uint32_t kv_base = smem_u32(sKV);
-      const uint32_t p_base = smem_u32(sP);
       auto issue_s = [&](int i, uint32_t kstage) {
         const uint32_t qa = q_base + i * C::kTileBytes;
         const uint32_t ka = kv_base + kstage * C::kTileBytes;
@@ -261,14 +261,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       auto issue_o = [&](int i, uint32_t vstage, bool acc) {
-        const uint32_t pa = p_base + i * C::kPBytes;
         const uint32_t va = kv_base + vstage * C::kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_bf16_ss(tmem + C::kColO + i * D, smem_desc_sw128(pa + aoff, 0, 1024),
-                      smem_desc_sw128(va + kk * 2048, 16384, 1024), idesc_o, (acc || kk > 0));
-        }
+        for (int kk = 0; kk < 8; ++kk)
+          mma_f16_ts(tmem + C::kColO + i * D, tmem + C::kColS + i * 128 + kk * 8,
+                     smem_desc_sw128(va + kk * 2048, 16384, 1024), idesc_o, (acc || kk > 0));
       };
       for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
         const WorkItem it = decode(p, w);
@@ -297,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (t == 0 && items > 0 && !(ok = mbar_wait(&bar_o_free[i], (items - 1) & 1, wc))) break;
             tc_fence_after();
             issue_o(i, sv, t > 0);
-            mma_commit(&bar_o_done[i]);
+            if (t + 1 == nt) mma_commit(&bar_o_done[i]);  // O_i final: the epilogue may read it
             if (i == 1) mma_commit(&bar_kv_empty[sv]);
             if (t + 1 < nt) {
               const uint32_t ck = kv_cnt + 2 * (t + 1), sk = ck % C::kStages;
@@ -326,7 +323,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const uint32_t s_col = lane_base + C::kColS + i * 128;
     const uint32_t o_col = lane_base + C::kColO + i * D;
-    const uint32_t p_row = smem_u32(sP + i * C::kPBytes);
     uint32_t s_cnt = 0, o_cnt = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
@@ -362,10 +358,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < 128; ++c)
               if (c >= lim) s[c] = -INFINITY;
           }
-          float mx = -INFINITY;
+          // Row max with eight independent chains (one warp per scheduler: keep
+          // the dependent-latency chains short).
+          float mx8[8];
 #pragma unroll
-          for (int c = 0; c < 128; ++c) mx = fmaxf(mx, s[c]);
-          mx *= p.scale_log2;
+          for (int j = 0; j < 8; ++j) mx8[j] = s[j];
+#pragma unroll
+          for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+          const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                 fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
+                           p.scale_log2;
           const float m_new = fmaxf(m_run, mx);
           const bool rescale = m_new > m_run + kRescaleThreshold;
           float alpha = 1.f;
@@ -374,41 +376,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             m_run = m_new;
           }
           const float m_use = m_run == -INFINITY ? 0.f : m_run;
-          float rowsum = 0.f;
+          // P = exp2(s * scale * log2e - m): fp16 pairs straight into TMEM columns
+          // [0, 64) of S_i, 64 score columns at a time.
+          float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int c = 0; c < 128; ++c) {
-            s[c] = ex2(fmaf(s[c], p.scale_log2, -m_use));
-            rowsum += s[c];
+          for (int h2 = 0; h2 < 2; ++h2) {
+            float pk[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float p0 = ex2(fmaf(s[64 * h2 + 2 * j], p.scale_log2, -m_use));
+              const float p1 = ex2(fmaf(s[64 * h2 + 2 * j + 1], p.scale_log2, -m_use));
+              rs[(2 * j) & 7] += p0;
+              rs[(2 * j + 1) & 7] += p1;
+              pk[j] = __uint_as_float(pack_f16(p0, p1));
+            }
+            tmem_st32(s_col + 32 * h2, pk);
           }
-          if (t > 0) {
-            // P buffer and O accumulator are free once P*V of the previous tile is done.
-            ok = mbar_wait(&bar_o_done[i], o_cnt & 1, wc);
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            ++o_cnt;
-            tc_fence_after();
-            if (__any_sync(0xffffffffu, rescale)) {
+          const float rowsum = ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
+          // P_i(t-1) V has completed (see above), so O_i can be rescaled now.
+          if (t > 0 && __any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
-              for (int c = 0; c < D / 32; ++c) {
-                float v[32];
-                tmem_ld32(o_col + c * 32, v);
-                tmem_ld_wait();
+            for (int c = 0; c < D / 32; ++c) {
+              float v[32];
+              tmem_ld32(o_col + c * 32, v);
+              tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] *= alpha;
-                tmem_st32(o_col + c * 32, v);
-              }
-              tmem_st_wait();
+              for (int j = 0; j < 32; ++j) v[j] *= alpha;
+              tmem_st32(o_col + c * 32, v);
             }
           }
           l = l * alpha + rowsum;
-          // P row r -> shared memory, two 64-key swizzled panels.
-#pragma unroll
-          for (int ch = 0; ch < 16; ++ch) {
-            const int c0 = ch * 8;
-            const uint32_t addr = p_row + (ch >> 3) * 16384 + sw128_offset(r, ch & 7);
-            st_shared_v4(addr, pack_f16(s[c0], s[c0 + 1]), pack_f16(s[c0 + 2], s[c0 + 3]),
-                         pack_f16(s[c0 + 4], s[c0 + 5]), pack_f16(s[c0 + 6], s[c0 + 7]));
-          }
-          fence_proxy_async_smem();
+          tmem_st_wait();
           tc_fence_before();
           mbar_arrive(&bar_p_ready[i]);
         }
