@@ -108,8 +108,8 @@ __device__ __forceinline__ void tma_reduce_add_3d(const void* tmap, const void* 
       : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read_le1() {
-  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void drain_group_sync() {  // the 128 threads of the dQ warpgroup
@@ -218,10 +218,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ++kv_items;
       const int nsteps = G * it.n_qt;
+      // L2 prefetches: the next unit's K/V tiles now, each step's Q/dO tiles
+      // two steps ahead, so the shared-memory loads above hit in L2.
+      if (lane == 0 && w + (int)gridDim.x < n_work) {
+        const BwdItem nx = decode(p, w + gridDim.x);
+        for (int pn = 0; pn < C::kPanels; ++pn) {
+          tma_prefetch_3d(nx.src ? &tm_kb : &tm_k, pn * 64, nx.g, nx.src_row);
+          tma_prefetch_3d(nx.src ? &tm_vb : &tm_v, pn * 64, nx.g, nx.src_row);
+        }
+      }
       for (int j = 0; j < nsteps; ++j) {
         const int h = it.g * G + j / it.n_qt;
         const int q0 = it.piece_start + (it.qt_first + j % it.n_qt) * 128;
         const int q_rows = min(128, it.piece_end - q0);
+        if (lane == 0 && j + 2 < nsteps) {
+          const int h2 = it.g * G + (j + 2) / it.n_qt;
+          const int q2 = it.piece_start + (it.qt_first + (j + 2) % it.n_qt) * 128;
+          for (int pn = 0; pn < C::kPanels; ++pn) {
+            tma_prefetch_3d(&tm_q, pn * 64, h2, q2);
+            tma_prefetch_3d(&tm_do, pn * 64, h2, q2);
+          }
+        }
         // Q tile and the rows' LSE / D into Q stage s.
         const int s = qc & 1;
         if (qc >= 2) {
@@ -400,10 +417,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t c = qc + j, s = c & 1;
         const int q0 = it.piece_start + (it.qt_first + j % it.n_qt) * 128;
         const int lim = key - q0 - 64 * half;  // local columns below lim cannot see this key
+        // Whole tile below the diagonal with 128 keys: no element needs a mask
+        // (query rows past the piece end have LSE = +inf, hence P = 0).
+        const bool unmasked = it.n == 128 && it.key0 + 127 <= q0;
         ok = mbar_wait(&bar_s_full, gstep & 1, wc) && mbar_wait(&bar_q_full[s], (c >> 1) & 1, wc);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
-        const float* st = stat + s * 256 + 64 * half;
+        const float4* st4 = reinterpret_cast<const float4*>(stat + s * 256 + 64 * half);
         uint32_t pk[32];
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
@@ -411,13 +431,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(s_cols + cc * 32, v);
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
+          for (int e = 0; e < 32; e += 4) {
             const int col = cc * 32 + e;
-            float p0 = ex2(fmaf(v[e], p.scale_log2, -st[col]));
-            float p1 = ex2(fmaf(v[e + 1], p.scale_log2, -st[col + 1]));
-            if (!key_valid || col < lim) p0 = 0.f;
-            if (!key_valid || col + 1 < lim) p1 = 0.f;
+            const float4 l4 = st4[col >> 2];
+            float p0 = ex2(fmaf(v[e], p.scale_log2, -l4.x));
+            float p1 = ex2(fmaf(v[e + 1], p.scale_log2, -l4.y));
+            float p2 = ex2(fmaf(v[e + 2], p.scale_log2, -l4.z));
+            float p3 = ex2(fmaf(v[e + 3], p.scale_log2, -l4.w));
+            if (!unmasked) {
+              if (!key_valid || col < lim) p0 = 0.f;
+              if (!key_valid || col + 1 < lim) p1 = 0.f;
+              if (!key_valid || col + 2 < lim) p2 = 0.f;
+              if (!key_valid || col + 3 < lim) p3 = 0.f;
+            }
             pk[col >> 1] = pack_f16(p0, p1);
+            pk[(col >> 1) + 1] = pack_f16(p2, p3);
           }
         }
         {
@@ -433,6 +461,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok && gstep > 0) ok = mbar_wait(&bar_ds_free, (gstep - 1) & 1, wc);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
+        // dS = P (dP - D) in packed fp16: (dP - D) and the product are each
+        // rounded to fp16, the operand type of the dK and dQ products.
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           float v[32];
@@ -440,11 +470,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_wait();
           uint32_t o[16];
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
+          for (int e = 0; e < 32; e += 4) {
             const int col = cc * 32 + e;
-            const uint32_t pp = pk[col >> 1];
-            o[e >> 1] = pack_f16(f16_lo(pp) * (v[e] - st[128 + col]),
-                                 f16_hi(pp) * (v[e + 1] - st[128 + col + 1]));
+            const float4 d4 = st4[32 + (col >> 2)];
+            const __half2 x01 = __floats2half2_rn(v[e] - d4.x, v[e + 1] - d4.y);
+            const __half2 x23 = __floats2half2_rn(v[e + 2] - d4.z, v[e + 3] - d4.w);
+            const uint32_t p01 = pk[col >> 1], p23 = pk[(col >> 1) + 1];
+            const __half2 r01 = __hmul2(*reinterpret_cast<const __half2*>(&p01), x01);
+            const __half2 r23 = __hmul2(*reinterpret_cast<const __half2*>(&p23), x23);
+            o[e >> 1] = *reinterpret_cast<const uint32_t*>(&r01);
+            o[(e >> 1) + 1] = *reinterpret_cast<const uint32_t*>(&r23);
           }
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4)
@@ -490,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     uint8_t* stage = smem + C::kStage;
-    uint32_t gstep = 0, chunks = 0;
+    uint32_t gstep = 0;
     bool ok = true;
     for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
       const BwdItem it = decode(p, w);
@@ -501,28 +536,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = drain_group_all(mbar_wait(&bar_dq_full, gstep & 1, wc));
         if (!ok) break;
         tc_fence_after();
+        // Two 32-column chunks at a time: both loads in flight together, the
+        // TMEM columns released as soon as every chunk has been read.
+        constexpr int kPairs = D / 64;
+        float a[32], b[32];
+        tmem_ld32(lane_base + C::kColDP, a);
+        tmem_ld32(lane_base + C::kColDP + 32, b);
+        tmem_ld_wait();
+        if (kPairs == 1) {
+          tc_fence_before();
+          mbar_arrive(&bar_dq_free);  // every dQ column of this step has been read
+        }
 #pragma unroll 1
-        for (int cc = 0; cc < D / 32; ++cc, ++chunks) {
-          float v[32];
-          tmem_ld32(lane_base + C::kColDP + cc * 32, v);
-          tmem_ld_wait();
-          if (cc == D / 32 - 1) {
-            tc_fence_before();
-            mbar_arrive(&bar_dq_free);  // every dQ column of this step is in registers
-          }
-          uint8_t* buf = stage + (chunks & 1) * 16384;
-          if (r == 0) bulk_wait_read_le1();  // the reduce that last read `buf` is done with it
+        for (int pr = 0; pr < kPairs; ++pr) {
+          if (r == 0) bulk_wait_read_all();  // earlier reduces are done reading the tiles
           drain_group_sync();
-          const uint32_t row = smem_u32(buf);
+          const uint32_t b0 = smem_u32(stage), b1 = smem_u32(stage + 16384);
 #pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4)
-            st_shared_v4(row + sw128_offset(r, q4), __float_as_uint(v[4 * q4] * p.scale),
-                         __float_as_uint(v[4 * q4 + 1] * p.scale), __float_as_uint(v[4 * q4 + 2] * p.scale),
-                         __float_as_uint(v[4 * q4 + 3] * p.scale));
+          for (int q4 = 0; q4 < 8; ++q4) {
+            st_shared_v4(b0 + sw128_offset(r, q4), __float_as_uint(a[4 * q4] * p.scale),
+                         __float_as_uint(a[4 * q4 + 1] * p.scale), __float_as_uint(a[4 * q4 + 2] * p.scale),
+                         __float_as_uint(a[4 * q4 + 3] * p.scale));
+            st_shared_v4(b1 + sw128_offset(r, q4), __float_as_uint(b[4 * q4] * p.scale),
+                         __float_as_uint(b[4 * q4 + 1] * p.scale), __float_as_uint(b[4 * q4 + 2] * p.scale),
+                         __float_as_uint(b[4 * q4 + 3] * p.scale));
+          }
+          if (pr + 1 < kPairs) {
+            tmem_ld32(lane_base + C::kColDP + 64 * (pr + 1), a);
+            tmem_ld32(lane_base + C::kColDP + 64 * (pr + 1) + 32, b);
+            tmem_ld_wait();
+            if (pr + 2 == kPairs) {
+              tc_fence_before();
+              mbar_arrive(&bar_dq_free);  // every dQ column of this step has been read
+            }
+          }
           fence_proxy_async_smem();
           drain_group_sync();
           if (r == 0) {
-            tma_reduce_add_3d(&tm_dq, buf, cc * 32, h, q0);
+            tma_reduce_add_3d(&tm_dq, stage, 64 * pr, h, q0);
+            tma_reduce_add_3d(&tm_dq, stage + 16384, 64 * pr + 32, h, q0);
             bulk_commit();
           }
         }
