@@ -71,9 +71,12 @@ __global__ void __launch_bounds__(kGatherThreads)
 // ------------------------------------------------------------------- merge
 // "LLM Context Parallel in Production", "Core Principle" / "Ring Attention":
 // LSE = ln sum_b exp(LSE_b), O = sum_b exp(LSE_b - LSE) O_b. One thread owns
-// four consecutive head-dim elements of one (row, head); parts whose LSE is
-// -inf (no key of that block visible) are not read.
+// four consecutive head-dim elements of one (row, head). All of a chunk's
+// LSE_b are read first, then every non-empty part's O_b is loaded at once (up
+// to kMergeChunk loads in flight per thread); parts whose LSE is -inf (no key
+// of that block visible) are not read.
 constexpr int kMergeThreads = 256;
+constexpr int kMergeChunk = 8;
 
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads)
@@ -82,38 +85,49 @@ __global__ void __launch_bounds__(kMergeThreads)
   constexpr int V = D / 4;  // float4 per (row, head)
   const int64_t total = rows * hq * V;
   const float kLog2e = 1.4426950408889634f;
+  const int64_t part_stride = rows * hq * V;  // float4 between consecutive parts
   for (int64_t idx = (int64_t)blockIdx.x * kMergeThreads + threadIdx.x; idx < total;
        idx += (int64_t)gridDim.x * kMergeThreads) {
     const int vec = (int)(idx % V);
     const int64_t rh = idx / V;
     const int h = (int)(rh % hq);
     const int64_t row = rh / hq;
+    const float* lp = lse_parts + (int64_t)h * rows + row;
+    const int64_t lstride = (int64_t)hq * rows;
     float m = -INFINITY;
-    for (int b = 0; b < B; ++b) m = fmaxf(m, __ldg(lse_parts + ((int64_t)b * hq + h) * rows + row));
+    for (int b = 0; b < B; ++b) m = fmaxf(m, __ldg(lp + b * lstride));
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float lse = -INFINITY;
+    float total_w = 0.f;
     if (m != -INFINITY) {
-      float total_w = 0.f;
-      for (int b = 0; b < B; ++b) {
-        const float lb = __ldg(lse_parts + ((int64_t)b * hq + h) * rows + row);
-        if (lb == -INFINITY) continue;
-        const float w = ex2f((lb - m) * kLog2e);
-        const float4 o = __ldg(o_parts + (((int64_t)b * rows + row) * hq + h) * V + vec);
-        total_w += w;
-        acc.x = fmaf(w, o.x, acc.x);
-        acc.y = fmaf(w, o.y, acc.y);
-        acc.z = fmaf(w, o.z, acc.z);
-        acc.w = fmaf(w, o.w, acc.w);
+      const float4* op = o_parts + rh * V + vec;
+      for (int b0 = 0; b0 < B; b0 += kMergeChunk) {
+        float w[kMergeChunk];
+        float4 o[kMergeChunk];
+#pragma unroll
+        for (int u = 0; u < kMergeChunk; ++u) {
+          const float lb = b0 + u < B ? __ldg(lp + (b0 + u) * lstride) : -INFINITY;
+          w[u] = lb == -INFINITY ? 0.f : ex2f((lb - m) * kLog2e);
+        }
+#pragma unroll
+        for (int u = 0; u < kMergeChunk; ++u)
+          o[u] = w[u] != 0.f ? __ldg(op + (b0 + u) * part_stride) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < kMergeChunk; ++u) {
+          total_w += w[u];
+          acc.x = fmaf(w[u], o[u].x, acc.x);
+          acc.y = fmaf(w[u], o[u].y, acc.y);
+          acc.z = fmaf(w[u], o[u].z, acc.z);
+          acc.w = fmaf(w[u], o[u].w, acc.w);
+        }
       }
       const float inv = 1.f / total_w;
       acc.x *= inv;
       acc.y *= inv;
       acc.z *= inv;
       acc.w *= inv;
-      lse = m + logf(total_w);
     }
-    out[(row * hq + h) * V + vec] = make_uint2(pack2(acc.x, acc.y), pack2(acc.z, acc.w));
-    if (vec == 0) lse_out[(int64_t)h * rows + row] = lse;
+    out[rh * V + vec] = make_uint2(pack2(acc.x, acc.y), pack2(acc.z, acc.w));
+    if (vec == 0) lse_out[(int64_t)h * rows + row] = m == -INFINITY ? -INFINITY : m + logf(total_w);
   }
 }
 
@@ -175,7 +189,8 @@ __global__ void __launch_bounds__(kPreThreads)
   for (int c = blockIdx.x; c < n_chunks; c += gridDim.x) {
     const int chunk = __ldg(order + c);
     const int r0 = __ldg(rows + 2 * chunk), nr = __ldg(rows + 2 * chunk + 1);
-    for (int pr = warp; pr < nr * hq; pr += kPreThreads / 32) {
+    for (int pr = warp + (kPreThreads / 32) * blockIdx.y; pr < nr * hq;
+         pr += (kPreThreads / 32) * gridDim.y) {
       const int r = r0 + pr / hq, h = pr % hq;
       const int64_t base = ((int64_t)r * hq + h) * D + lane * E;
       uint32_t b[W], x[W], oq[W], od[W];
@@ -280,7 +295,7 @@ int launch_bwd_preprocess(const void* out, bool out_f32, const void* dout, const
                           int32_t hq, int32_t d, float* delta, float* dq, void* q16, void* do16,
                           int* err, cudaStream_t st) {
   if (n_chunks == 0) return FCP_OK;
-  const int grid = n_chunks;
+  const dim3 grid(n_chunks, 8);  // a chunk's (row, head) pairs spread over 8 blocks
   using B = __nv_bfloat16;
   auto go = [&](auto kernel) {
     kernel<<<grid, kPreThreads, 0, st>>>(out, static_cast<const B*>(dout), static_cast<const B*>(q),

@@ -171,12 +171,14 @@ def attention_per_doc(q, k, v, cu, scale=None, docs=None, heads=None,
     return o, lse
 
 
-def attention_rows(q, k, v, cu, rows, heads, scale=None):
+def attention_rows(q, k, v, cu, rows, heads, scale=None, q_holds_rows=False):
     """Forward for a sample of (query row, head) pairs: the full definition per
     row, for spot checks at sizes where whole documents are too costly.
-    Returns o [len(rows), len(heads), d] and lse [len(heads), len(rows)]."""
+    With q_holds_rows, q[a] is the query of row rows[a] (only the sampled rows
+    are passed). Returns o [len(rows), len(heads), d] and lse
+    [len(heads), len(rows)]."""
     q, k, v = to_f64(q), to_f64(k), to_f64(v)
-    T, Hq, d = q.shape
+    _, Hq, d = q.shape
     G = _group(Hq, k.shape[1])
     scale = default_scale(d) if scale is None else scale
     cu = np.asarray(cu, dtype=np.int64)
@@ -186,9 +188,10 @@ def attention_rows(q, k, v, cu, rows, heads, scale=None):
     lse = np.zeros((len(heads), len(rows)))
     for a, i in enumerate(rows):
         s0 = int(cu[doc[i]])
+        qi = q[a] if q_holds_rows else q[i]
         for b, h in enumerate(heads):
             g = h // G
-            s = scale * (k[s0:i + 1, g] @ q[i, h])
+            s = scale * (k[s0:i + 1, g] @ qi[h])
             m = s.max()
             e = np.exp(s - m)
             lse[b, a] = m + math.log(e.sum())

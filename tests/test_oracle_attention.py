@@ -204,3 +204,6 @@ def test_rows_sampler_matches_per_doc():
     os_, ls = A.attention_rows(q, k, v, cu, rows, heads)
     np.testing.assert_allclose(os_, o[rows][:, heads], atol=1e-12, rtol=0)
     np.testing.assert_allclose(ls, lse[heads][:, rows], atol=1e-12, rtol=0)
+    os2, ls2 = A.attention_rows(q[rows], k, v, cu, rows, heads, q_holds_rows=True)
+    np.testing.assert_array_equal(os2, os_)
+    np.testing.assert_array_equal(ls2, ls)
