@@ -4,6 +4,8 @@
 // All three move contiguous rows with 128-bit loads and stores, several
 // independent loads in flight per thread, and grids sized in multiples of the
 // SM count.
+#include <algorithm>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -70,64 +72,77 @@ __global__ void __launch_bounds__(kGatherThreads)
 
 // ------------------------------------------------------------------- merge
 // "LLM Context Parallel in Production", "Core Principle" / "Ring Attention":
-// LSE = ln sum_b exp(LSE_b), O = sum_b exp(LSE_b - LSE) O_b. One thread owns
-// four consecutive head-dim elements of one (row, head). All of a chunk's
-// LSE_b are read first, then every non-empty part's O_b is loaded at once (up
-// to kMergeChunk loads in flight per thread); parts whose LSE is -inf (no key
-// of that block visible) are not read.
+// LSE = ln sum_b exp(LSE_b), O = sum_b exp(LSE_b - LSE) O_b. A group of
+// D/4 lanes owns one (row, head): lane b first computes part b's weight
+// (its LSE read once, the max and sum reduced across the group), the weights
+// are shuffled to every lane, and each lane then streams one float4 of every
+// non-empty part, four parts' loads in flight at a time. Parts whose LSE is
+// -inf (no key of that block visible) are not read. B <= D/4 (one lane per part).
 constexpr int kMergeThreads = 256;
-constexpr int kMergeChunk = 8;
 
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads)
     merge_kernel(const float4* __restrict__ o_parts, const float* __restrict__ lse_parts, int B,
-                 int64_t rows, int hq, uint2* __restrict__ out, float* __restrict__ lse_out) {
-  constexpr int V = D / 4;  // float4 per (row, head)
-  const int64_t total = rows * hq * V;
+                 int rows, int hq, uint2* __restrict__ out, float* __restrict__ lse_out) {
+  constexpr int V = D / 4;              // lanes (float4) per (row, head): 32 or 16
+  constexpr int kUnitsPerWarp = 32 / V;
   const float kLog2e = 1.4426950408889634f;
-  const int64_t part_stride = rows * hq * V;  // float4 between consecutive parts
-  for (int64_t idx = (int64_t)blockIdx.x * kMergeThreads + threadIdx.x; idx < total;
-       idx += (int64_t)gridDim.x * kMergeThreads) {
-    const int vec = (int)(idx % V);
-    const int64_t rh = idx / V;
-    const int h = (int)(rh % hq);
-    const int64_t row = rh / hq;
-    const float* lp = lse_parts + (int64_t)h * rows + row;
-    const int64_t lstride = (int64_t)hq * rows;
-    float m = -INFINITY;
-    for (int b = 0; b < B; ++b) m = fmaxf(m, __ldg(lp + b * lstride));
+  const int lane = threadIdx.x & 31;
+  const int vec = lane & (V - 1);
+  const int sub = lane / V;             // which unit of the warp
+  const int h = blockIdx.y;             // one query head per grid row
+  const unsigned gmask = V == 32 ? 0xffffffffu : (0xffffu << (16 * sub));
+  const int64_t lstride = (int64_t)hq * rows;
+  const int64_t part_stride = (int64_t)rows * hq * V;  // float4 between consecutive parts
+  const float* lse_h = lse_parts + (int64_t)h * rows;
+  const int step = gridDim.x * (kMergeThreads / 32) * kUnitsPerWarp;
+  // Rows of one head: neighbouring warps share LSE cache lines. The next
+  // row's LSE is fetched while this row's O parts are in flight.
+  int row = (blockIdx.x * (kMergeThreads / 32) + (threadIdx.x >> 5)) * kUnitsPerWarp + sub;
+  float lb_next = (row < rows && vec < B) ? __ldg(lse_h + vec * lstride + row) : -INFINITY;
+  for (; row - sub < rows; row += step) {
+    const bool live = row < rows;
+    const float lb = lb_next;
+    const int nrow = row + step;
+    lb_next = (nrow < rows && vec < B) ? __ldg(lse_h + vec * lstride + nrow) : -INFINITY;
+    float m = lb;
+#pragma unroll
+    for (int o = V / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(gmask, m, o));
+    const float wv = (lb == -INFINITY) ? 0.f : ex2f((lb - m) * kLog2e);
+    float tw = wv;
+#pragma unroll
+    for (int o = V / 2; o > 0; o >>= 1) tw += __shfl_xor_sync(gmask, tw, o);
+    const int64_t unit = (int64_t)row * hq + h;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float total_w = 0.f;
-    if (m != -INFINITY) {
-      const float4* op = o_parts + rh * V + vec;
-      for (int b0 = 0; b0 < B; b0 += kMergeChunk) {
-        float w[kMergeChunk];
-        float4 o[kMergeChunk];
+    if (live && m != -INFINITY) {
+      const float4* op = o_parts + unit * V + vec;
+      for (int b0 = 0; b0 < B; b0 += 4) {
+        float w[4];
+        float4 o[4];
 #pragma unroll
-        for (int u = 0; u < kMergeChunk; ++u) {
-          const float lb = b0 + u < B ? __ldg(lp + (b0 + u) * lstride) : -INFINITY;
-          w[u] = lb == -INFINITY ? 0.f : ex2f((lb - m) * kLog2e);
-        }
+        for (int k = 0; k < 4; ++k) w[k] = __shfl_sync(gmask, wv, (sub * V) + ((b0 + k) & (V - 1)));
 #pragma unroll
-        for (int u = 0; u < kMergeChunk; ++u)
-          o[u] = w[u] != 0.f ? __ldg(op + (b0 + u) * part_stride) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 0; k < 4; ++k)
+          o[k] = (b0 + k < B && w[k] != 0.f) ? __ldg(op + (b0 + k) * part_stride) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int u = 0; u < kMergeChunk; ++u) {
-          total_w += w[u];
-          acc.x = fmaf(w[u], o[u].x, acc.x);
-          acc.y = fmaf(w[u], o[u].y, acc.y);
-          acc.z = fmaf(w[u], o[u].z, acc.z);
-          acc.w = fmaf(w[u], o[u].w, acc.w);
+        for (int k = 0; k < 4; ++k) {
+          const float ww = b0 + k < B ? w[k] : 0.f;
+          acc.x = fmaf(ww, o[k].x, acc.x);
+          acc.y = fmaf(ww, o[k].y, acc.y);
+          acc.z = fmaf(ww, o[k].z, acc.z);
+          acc.w = fmaf(ww, o[k].w, acc.w);
         }
       }
-      const float inv = 1.f / total_w;
+      const float inv = 1.f / tw;
       acc.x *= inv;
       acc.y *= inv;
       acc.z *= inv;
       acc.w *= inv;
     }
-    out[rh * V + vec] = make_uint2(pack2(acc.x, acc.y), pack2(acc.z, acc.w));
-    if (vec == 0) lse_out[(int64_t)h * rows + row] = m == -INFINITY ? -INFINITY : m + logf(total_w);
+    if (live) {
+      out[unit * V + vec] = make_uint2(pack2(acc.x, acc.y), pack2(acc.z, acc.w));
+      if (vec == 0) lse_out[(int64_t)h * rows + row] = m == -INFINITY ? -INFINITY : m + logf(tw);
+    }
   }
 }
 
@@ -276,17 +291,18 @@ int launch_gather(const void* k, const void* v, const int32_t* tasks, int32_t n_
 int launch_merge(const float* o_parts, const float* lse_parts, int32_t B, int64_t rows, int32_t hq,
                  int32_t d, void* out, float* lse_out, int num_sms, cudaStream_t st) {
   if (rows == 0) return FCP_OK;
-  const int64_t total = rows * hq * (d / 4);
-  int64_t grid = (total + kMergeThreads - 1) / kMergeThreads;
-  if (grid > (int64_t)num_sms * 64) grid = (int64_t)num_sms * 64;
+  if (B > d / 4 || rows * hq >= (int64_t(1) << 30)) return FCP_ERR_UNSUPPORTED;  // one lane per part
+  const int units_per_block = (kMergeThreads / 32) * (d == 128 ? 1 : 2);
+  int64_t gx = (rows + units_per_block - 1) / units_per_block;
+  const int64_t cap = std::max<int64_t>(1, (int64_t)num_sms * 32 / hq);
+  if (gx > cap) gx = cap;
+  const dim3 grid((unsigned)gx, (unsigned)hq);
   if (d == 128)
-    merge_kernel<128><<<(int)grid, kMergeThreads, 0, st>>>(
-        reinterpret_cast<const float4*>(o_parts), lse_parts, B, rows, hq, static_cast<uint2*>(out),
-        lse_out);
+    merge_kernel<128><<<grid, kMergeThreads, 0, st>>>(reinterpret_cast<const float4*>(o_parts), lse_parts,
+                                                      B, (int)rows, hq, static_cast<uint2*>(out), lse_out);
   else
-    merge_kernel<64><<<(int)grid, kMergeThreads, 0, st>>>(
-        reinterpret_cast<const float4*>(o_parts), lse_parts, B, rows, hq, static_cast<uint2*>(out),
-        lse_out);
+    merge_kernel<64><<<grid, kMergeThreads, 0, st>>>(reinterpret_cast<const float4*>(o_parts), lse_parts,
+                                                     B, (int)rows, hq, static_cast<uint2*>(out), lse_out);
   return cudaGetLastError() == cudaSuccess ? FCP_OK : FCP_ERR_CUDA;
 }
 

@@ -228,6 +228,8 @@ int fcp_attn_fwd(const void* q, const void* k, const void* v, const void* kbuf,
  *   o_parts   fp32 [B][rows][hq][d]; lse_parts fp32 [B][hq][rows].
  *   out       bf16 [rows][hq][d]; lse_out fp32 [hq][rows].
  * A row empty in every block (all LSE_b = -inf) gets O = 0, LSE = -inf.
+ * Limits: 1 <= B <= d/4 (32 for d = 128, 16 for d = 64), rows * hq < 2^30
+ * (FCP_ERR_UNSUPPORTED otherwise).
  */
 int fcp_merge(const float* o_parts, const float* lse_parts, int32_t B, int64_t rows,
               int32_t hq, int32_t d, void* out, float* lse_out, void* stream);
