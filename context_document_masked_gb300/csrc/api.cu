@@ -335,6 +335,7 @@ int fcp_merge(const float* o_parts, const float* lse_parts, int32_t B, int64_t r
               int32_t d, void* out, float* lse_out, void* stream) {
   if (B < 1 || rows < 0 || hq < 1) return FCP_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FCP_ERR_UNSUPPORTED;
+  if (B > d / 4 || rows * hq >= (int64_t(1) << 30)) return FCP_ERR_UNSUPPORTED;
   if (rows == 0) return FCP_OK;
   if (!o_parts || !lse_parts || !out || !lse_out) return FCP_ERR_INVALID_ARG;
   if (!aligned16(o_parts) || !aligned16(out)) return FCP_ERR_INVALID_ARG;

@@ -72,76 +72,84 @@ __global__ void __launch_bounds__(kGatherThreads)
 
 // ------------------------------------------------------------------- merge
 // "LLM Context Parallel in Production", "Core Principle" / "Ring Attention":
-// LSE = ln sum_b exp(LSE_b), O = sum_b exp(LSE_b - LSE) O_b. A group of
-// D/4 lanes owns one (row, head): lane b first computes part b's weight
-// (its LSE read once, the max and sum reduced across the group), the weights
-// are shuffled to every lane, and each lane then streams one float4 of every
-// non-empty part, four parts' loads in flight at a time. Parts whose LSE is
-// -inf (no key of that block visible) are not read. B <= D/4 (one lane per part).
+// LSE = ln sum_b exp(LSE_b), O = sum_b exp(LSE_b - LSE) O_b.
+//
+// A warp takes G = 32 / BP consecutive rows of one head (BP = B rounded up to
+// a power of two). Weight phase: lane (u, b) reads part b's LSE of row u, the
+// max and the sum reduce over BP lanes (log2 BP shuffles), and each lane keeps
+// its normalised weight exp(LSE_b - LSE); lane (u, 0) writes LSE. Data phase:
+// row by row, D/4 lanes stream one float4 each of every non-empty part (four
+// parts' loads in flight at a time) with the weight shuffled from lane (u, b).
+// Parts whose LSE is -inf (no key of that block visible) are not read.
 constexpr int kMergeThreads = 256;
 
-template <int D>
+template <int D, int BP>
 __global__ void __launch_bounds__(kMergeThreads)
     merge_kernel(const float4* __restrict__ o_parts, const float* __restrict__ lse_parts, int B,
                  int rows, int hq, uint2* __restrict__ out, float* __restrict__ lse_out) {
-  constexpr int V = D / 4;              // lanes (float4) per (row, head): 32 or 16
-  constexpr int kUnitsPerWarp = 32 / V;
+  constexpr int V = D / 4;               // lanes (float4) per (row, head): 32 or 16
+  constexpr int kRowsPerPass = 32 / V;   // rows one data pass covers
+  constexpr int G = 32 / BP;             // rows per weight phase
+  static_assert(G >= kRowsPerPass, "B too large for this head dimension");
   const float kLog2e = 1.4426950408889634f;
   const int lane = threadIdx.x & 31;
-  const int vec = lane & (V - 1);
-  const int sub = lane / V;             // which unit of the warp
-  const int h = blockIdx.y;             // one query head per grid row
-  const unsigned gmask = V == 32 ? 0xffffffffu : (0xffffu << (16 * sub));
+  const int wu = lane / BP, wb = lane % BP;   // weight phase: row in the group, part
+  const int vec = lane % V, sub = lane / V;   // data phase: float4 of the row, row in the pass
+  const int h = blockIdx.y;                   // one query head per grid row
   const int64_t lstride = (int64_t)hq * rows;
   const int64_t part_stride = (int64_t)rows * hq * V;  // float4 between consecutive parts
   const float* lse_h = lse_parts + (int64_t)h * rows;
-  const int step = gridDim.x * (kMergeThreads / 32) * kUnitsPerWarp;
-  // Rows of one head: neighbouring warps share LSE cache lines. The next
-  // row's LSE is fetched while this row's O parts are in flight.
-  int row = (blockIdx.x * (kMergeThreads / 32) + (threadIdx.x >> 5)) * kUnitsPerWarp + sub;
-  float lb_next = (row < rows && vec < B) ? __ldg(lse_h + vec * lstride + row) : -INFINITY;
-  for (; row - sub < rows; row += step) {
-    const bool live = row < rows;
-    const float lb = lb_next;
-    const int nrow = row + step;
-    lb_next = (nrow < rows && vec < B) ? __ldg(lse_h + vec * lstride + nrow) : -INFINITY;
-    float m = lb;
+  float* lse_o = lse_out + (int64_t)h * rows;
+  const int rstep = gridDim.x * (kMergeThreads / 32) * G;
+  int r0 = (blockIdx.x * (kMergeThreads / 32) + (threadIdx.x >> 5)) * G;
+  // Neighbouring warps read neighbouring rows of the same LSE lines; the next
+  // group's LSEs are fetched while this group's O parts stream.
+  auto lse_at = [&](int base) {
+    const int r = base + wu;
+    return (r < rows && wb < B) ? __ldg(lse_h + wb * lstride + r) : -INFINITY;
+  };
+  float l_next = lse_at(r0);
+  for (; r0 < rows; r0 += rstep) {
+    const float l = l_next;
+    l_next = lse_at(r0 + rstep);
+    float m = l;
 #pragma unroll
-    for (int o = V / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(gmask, m, o));
-    const float wv = (lb == -INFINITY) ? 0.f : ex2f((lb - m) * kLog2e);
-    float tw = wv;
+    for (int o = 1; o < BP; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float w = (l == -INFINITY) ? 0.f : ex2f((l - m) * kLog2e);
+    float tw = w;
 #pragma unroll
-    for (int o = V / 2; o > 0; o >>= 1) tw += __shfl_xor_sync(gmask, tw, o);
-    const int64_t unit = (int64_t)row * hq + h;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (live && m != -INFINITY) {
-      const float4* op = o_parts + unit * V + vec;
+    for (int o = 1; o < BP; o <<= 1) tw += __shfl_xor_sync(0xffffffffu, tw, o);
+    // A row with no visible key anywhere (all parts empty) has m = -inf:
+    // zero output and LSE -inf.
+    w = (m == -INFINITY) ? 0.f : w * (1.f / tw);
+    if (wb == 0 && r0 + wu < rows) lse_o[r0 + wu] = (m == -INFINITY) ? -INFINITY : m + logf(tw);
+#pragma unroll 2
+    for (int u0 = 0; u0 < G; u0 += kRowsPerPass) {
+      const int u = u0 + sub;
+      const int row = r0 + u;
+      const float4* op = o_parts + ((int64_t)row * hq + h) * V + vec;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int b0 = 0; b0 < B; b0 += 4) {
-        float w[4];
+        float wk[4];
         float4 o[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) w[k] = __shfl_sync(gmask, wv, (sub * V) + ((b0 + k) & (V - 1)));
+        for (int k = 0; k < 4; ++k) {
+          const float x = __shfl_sync(0xffffffffu, w, u * BP + ((b0 + k) % BP));
+          wk[k] = b0 + k < B ? x : 0.f;
+        }
+        // wk != 0 implies row < rows and part b0 + k non-empty.
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          o[k] = (b0 + k < B && w[k] != 0.f) ? __ldg(op + (b0 + k) * part_stride) : make_float4(0.f, 0.f, 0.f, 0.f);
+          o[k] = wk[k] != 0.f ? __ldg(op + (b0 + k) * part_stride) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const float ww = b0 + k < B ? w[k] : 0.f;
-          acc.x = fmaf(ww, o[k].x, acc.x);
-          acc.y = fmaf(ww, o[k].y, acc.y);
-          acc.z = fmaf(ww, o[k].z, acc.z);
-          acc.w = fmaf(ww, o[k].w, acc.w);
+          acc.x = fmaf(wk[k], o[k].x, acc.x);
+          acc.y = fmaf(wk[k], o[k].y, acc.y);
+          acc.z = fmaf(wk[k], o[k].z, acc.z);
+          acc.w = fmaf(wk[k], o[k].w, acc.w);
         }
       }
-      const float inv = 1.f / tw;
-      acc.x *= inv;
-      acc.y *= inv;
-      acc.z *= inv;
-      acc.w *= inv;
-    }
-    if (live) {
-      out[unit * V + vec] = make_uint2(pack2(acc.x, acc.y), pack2(acc.z, acc.w));
-      if (vec == 0) lse_out[(int64_t)h * rows + row] = m == -INFINITY ? -INFINITY : m + logf(tw);
+      if (row < rows) out[((int64_t)row * hq + h) * V + vec] = make_uint2(pack2(acc.x, acc.y), pack2(acc.z, acc.w));
     }
   }
 }
@@ -291,18 +299,35 @@ int launch_gather(const void* k, const void* v, const int32_t* tasks, int32_t n_
 int launch_merge(const float* o_parts, const float* lse_parts, int32_t B, int64_t rows, int32_t hq,
                  int32_t d, void* out, float* lse_out, int num_sms, cudaStream_t st) {
   if (rows == 0) return FCP_OK;
-  if (B > d / 4 || rows * hq >= (int64_t(1) << 30)) return FCP_ERR_UNSUPPORTED;  // one lane per part
-  const int units_per_block = (kMergeThreads / 32) * (d == 128 ? 1 : 2);
-  int64_t gx = (rows + units_per_block - 1) / units_per_block;
+  if (B > d / 4 || rows * hq >= (int64_t(1) << 30)) return FCP_ERR_UNSUPPORTED;
+  int bp = 1;
+  while (bp < B) bp *= 2;
+  const int64_t rows_per_block = (kMergeThreads / 32) * (32 / bp);
+  int64_t gx = (rows + rows_per_block - 1) / rows_per_block;
   const int64_t cap = std::max<int64_t>(1, (int64_t)num_sms * 32 / hq);
   if (gx > cap) gx = cap;
   const dim3 grid((unsigned)gx, (unsigned)hq);
-  if (d == 128)
-    merge_kernel<128><<<grid, kMergeThreads, 0, st>>>(reinterpret_cast<const float4*>(o_parts), lse_parts,
-                                                      B, (int)rows, hq, static_cast<uint2*>(out), lse_out);
-  else
-    merge_kernel<64><<<grid, kMergeThreads, 0, st>>>(reinterpret_cast<const float4*>(o_parts), lse_parts,
-                                                     B, (int)rows, hq, static_cast<uint2*>(out), lse_out);
+  const float4* op = reinterpret_cast<const float4*>(o_parts);
+  uint2* o = static_cast<uint2*>(out);
+  auto go = [&](auto kernel) { kernel<<<grid, kMergeThreads, 0, st>>>(op, lse_parts, B, (int)rows, hq, o, lse_out); };
+  if (d == 128) {
+    switch (bp) {
+      case 1: go(merge_kernel<128, 1>); break;
+      case 2: go(merge_kernel<128, 2>); break;
+      case 4: go(merge_kernel<128, 4>); break;
+      case 8: go(merge_kernel<128, 8>); break;
+      case 16: go(merge_kernel<128, 16>); break;
+      default: go(merge_kernel<128, 32>); break;
+    }
+  } else {
+    switch (bp) {
+      case 1: go(merge_kernel<64, 1>); break;
+      case 2: go(merge_kernel<64, 2>); break;
+      case 4: go(merge_kernel<64, 4>); break;
+      case 8: go(merge_kernel<64, 8>); break;
+      default: go(merge_kernel<64, 16>); break;
+    }
+  }
   return cudaGetLastError() == cudaSuccess ? FCP_OK : FCP_ERR_CUDA;
 }
 

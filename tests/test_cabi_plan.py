@@ -90,6 +90,11 @@ def test_device_calls_validate_before_launch(lib):
     assert st == lib.ERR_INVALID_ARG      # null plan checked first
     assert lib.raw_call("fcp_merge", None, None, 0, 10, 4, 128, None, None, None) == lib.ERR_INVALID_ARG
     assert lib.raw_call("fcp_merge", None, None, 2, 10, 4, 96, None, None, None) == lib.ERR_UNSUPPORTED
+    # At most d/4 parts (one lane per part in the weight phase), < 2^30 (row, head) pairs.
+    assert lib.raw_call("fcp_merge", None, None, 33, 10, 4, 128, None, None, None) == lib.ERR_UNSUPPORTED
+    assert lib.raw_call("fcp_merge", None, None, 17, 10, 4, 64, None, None, None) == lib.ERR_UNSUPPORTED
+    assert lib.raw_call("fcp_merge", None, None, 32, 10, 4, 128, None, None, None) == lib.ERR_INVALID_ARG
+    assert lib.raw_call("fcp_merge", None, None, 2, 1 << 28, 4, 128, None, None, None) == lib.ERR_UNSUPPORTED
     assert lib.raw_call("fcp_get_device_status", None, None) == lib.ERR_INVALID_ARG
     assert lib.workspace_bytes(lib.dims(1000, 8, 2, 128)) >= 256 + 8 * 1000 * 4 + 2 * 1000 * 8 * 128 * 2
     assert lib.strerror(lib.ERR_TIMEOUT) == "bounded device wait expired"

@@ -156,10 +156,17 @@ def test_partial_blocks_and_merge(cuda, case):
     assert _maxabs(lse.cpu(), lse_ref, "LSE") <= TOL_LSE
 
 
-def test_merge_kernel_against_oracle(cuda):
+MERGE_CASES = [(1, 128), (2, 128), (3, 128), (4, 128), (5, 128), (8, 128), (13, 128), (32, 128),
+               (1, 64), (2, 64), (4, 64), (7, 64), (16, 64)]
+
+
+@pytest.mark.parametrize("B,d", MERGE_CASES, ids=[f"B{b}-d{d}" for b, d in MERGE_CASES])
+def test_merge_kernel_against_oracle(cuda, B, d):
+    """Every part count the kernel specialises on (B rounded up to a power of
+    two, up to d/4), with a row count that leaves a ragged last row group."""
     from context_document_masked_gb300 import fcp
-    g = torch.Generator().manual_seed(3)
-    B, rows, hq, d = 5, 777, 4, 128
+    g = torch.Generator().manual_seed(3 + B)
+    rows, hq = 777, 4
     o_parts = torch.randn(B, rows, hq, d, generator=g)
     l_parts = torch.randn(B, hq, rows, generator=g) * 3
     mask = torch.rand(B, hq, rows, generator=g) < 0.3
