@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(kMergeThreads)
 // D_i = <dO_i, O_i> (the row term of dS = P (dP - D)), dQ rows zeroed so the
 // backward kernel can accumulate into them, and fp16 copies of Q and dO (the
 // backward's tensor-core operands; exact for bf16 values inside the fp16
-// range, error bit 4 otherwise). One warp per (row, head).
+// range, error bit 4 otherwise).
 constexpr int kPreThreads = 256;
 
 __device__ __forceinline__ uint32_t cvt_pair(uint32_t x, bool& ovf) {
@@ -168,36 +168,6 @@ __device__ __forceinline__ uint32_t cvt_pair(uint32_t x, bool& ovf) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// The forward output O, as bf16 or fp32: four (or two) consecutive elements
-// of one row, widened to fp32.
-template <int E, bool F32>
-__device__ __forceinline__ void load_o(const void* out, int64_t base, float (&o)[E]) {
-  if constexpr (F32) {
-    const float* p = static_cast<const float*>(out) + base;
-    if constexpr (E == 4) {
-      const float4 x = *reinterpret_cast<const float4*>(p);
-      o[0] = x.x; o[1] = x.y; o[2] = x.z; o[3] = x.w;
-    } else {
-      const float2 x = *reinterpret_cast<const float2*>(p);
-      o[0] = x.x; o[1] = x.y;
-    }
-  } else {
-    const __nv_bfloat16* p = static_cast<const __nv_bfloat16*>(out) + base;
-    uint32_t w[E / 2];
-    if constexpr (E == 4) {
-      const uint2 x = *reinterpret_cast<const uint2*>(p);
-      w[0] = x.x; w[E / 2 - 1] = x.y;
-    } else {
-      w[0] = *reinterpret_cast<const uint32_t*>(p);
-    }
-#pragma unroll
-    for (int i = 0; i < E / 2; ++i) {
-      o[2 * i] = __uint_as_float(w[i] << 16);
-      o[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
-  }
-}
-
 template <int D, bool OF32>
 __global__ void __launch_bounds__(kPreThreads)
     preprocess_kernel(const void* __restrict__ out, const __nv_bfloat16* __restrict__ dout,
@@ -205,48 +175,66 @@ __global__ void __launch_bounds__(kPreThreads)
                       const int32_t* __restrict__ order, int n_chunks, int T, int hq,
                       float* __restrict__ delta, float* __restrict__ dq, __half* __restrict__ q16,
                       __half* __restrict__ do16, int* __restrict__ err) {
-  constexpr int E = D / 32;  // elements per lane (4 or 2)
-  constexpr int W = E / 2;   // 32-bit words per lane
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // A chunk's rows, all heads, are one contiguous [rows][hq][D] block. Each
+  // thread takes 8 consecutive elements (16-byte loads of dO and Q, 16 or 32
+  // bytes of O); L = D / 8 lanes hold one (row, head) and reduce its D_i.
+  constexpr int L = D / 8;
+  const int lane = threadIdx.x & 31;
+  const int stride = kPreThreads * gridDim.y;
   bool ovf = false;
   for (int c = blockIdx.x; c < n_chunks; c += gridDim.x) {
     const int chunk = __ldg(order + c);
     const int r0 = __ldg(rows + 2 * chunk), nr = __ldg(rows + 2 * chunk + 1);
-    for (int pr = warp + (kPreThreads / 32) * blockIdx.y; pr < nr * hq;
-         pr += (kPreThreads / 32) * gridDim.y) {
-      const int r = r0 + pr / hq, h = pr % hq;
-      const int64_t base = ((int64_t)r * hq + h) * D + lane * E;
-      uint32_t b[W], x[W], oq[W], od[W];
-      float o[E];
-      load_o<E, OF32>(out, base, o);
-      if (W == 2) {
-        const uint2 vb = *reinterpret_cast<const uint2*>(dout + base);
-        const uint2 vx = *reinterpret_cast<const uint2*>(q + base);
-        b[0] = vb.x; b[W - 1] = vb.y; x[0] = vx.x; x[W - 1] = vx.y;
-      } else {
-        b[0] = *reinterpret_cast<const uint32_t*>(dout + base);
-        x[0] = *reinterpret_cast<const uint32_t*>(q + base);
+    const int total = nr * hq * L;  // 16-byte groups of the chunk
+    const int64_t e0 = (int64_t)r0 * hq * D;
+    // Warp-uniform trip count: every lane of a warp takes part in the
+    // shuffles; lanes past the end hold s = 0 and store nothing.
+    for (int g = threadIdx.x + kPreThreads * blockIdx.y; g - lane < total; g += stride) {
+      const bool live = g < total;
+      const int64_t base = e0 + (int64_t)g * 8;
+      uint4 b = make_uint4(0, 0, 0, 0), x = b;
+      float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (live) {
+        b = __ldg(reinterpret_cast<const uint4*>(dout + base));
+        x = __ldg(reinterpret_cast<const uint4*>(q + base));
+        if constexpr (OF32) {
+          const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(out) + base);
+          const float4 a0 = __ldg(p), a1 = __ldg(p + 1);
+          o[0] = a0.x; o[1] = a0.y; o[2] = a0.z; o[3] = a0.w;
+          o[4] = a1.x; o[5] = a1.y; o[6] = a1.z; o[7] = a1.w;
+        } else {
+          const uint4 w = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(out) + base));
+          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            o[2 * i] = __uint_as_float(ws[i] << 16);
+            o[2 * i + 1] = __uint_as_float(ws[i] & 0xFFFF0000u);
+          }
+        }
       }
+      const uint32_t bw[4] = {b.x, b.y, b.z, b.w}, xw[4] = {x.x, x.y, x.z, x.w};
+      uint32_t oq[4], od[4];
       float s = 0.f;
 #pragma unroll
-      for (int i = 0; i < W; ++i) {
-        s = fmaf(o[2 * i], __uint_as_float(b[i] << 16), s);
-        s = fmaf(o[2 * i + 1], __uint_as_float(b[i] & 0xFFFF0000u), s);
-        oq[i] = cvt_pair(x[i], ovf);
-        od[i] = cvt_pair(b[i], ovf);
+      for (int i = 0; i < 4; ++i) {
+        s = fmaf(o[2 * i], __uint_as_float(bw[i] << 16), s);
+        s = fmaf(o[2 * i + 1], __uint_as_float(bw[i] & 0xFFFF0000u), s);
+        oq[i] = cvt_pair(xw[i], ovf);
+        od[i] = cvt_pair(bw[i], ovf);
       }
-      if (W == 2) {
-        *reinterpret_cast<uint2*>(q16 + base) = make_uint2(oq[0], oq[W - 1]);
-        *reinterpret_cast<uint2*>(do16 + base) = make_uint2(od[0], od[W - 1]);
-        *reinterpret_cast<float4*>(dq + base) = make_float4(0.f, 0.f, 0.f, 0.f);
-      } else {
-        *reinterpret_cast<uint32_t*>(q16 + base) = oq[0];
-        *reinterpret_cast<uint32_t*>(do16 + base) = od[0];
-        *reinterpret_cast<float2*>(dq + base) = make_float2(0.f, 0.f);
+      if (live) {
+        *reinterpret_cast<uint4*>(q16 + base) = make_uint4(oq[0], oq[1], oq[2], oq[3]);
+        *reinterpret_cast<uint4*>(do16 + base) = make_uint4(od[0], od[1], od[2], od[3]);
+        float4* z = reinterpret_cast<float4*>(dq + base);
+        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      if (lane == 0) delta[(int64_t)h * T + r] = s;
+      for (int m = L / 2; m > 0; m >>= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
+      if (live && (g % L) == 0) {
+        const int u = g / L;  // (row, head) within the chunk
+        delta[(int64_t)(u % hq) * T + r0 + u / hq] = s;
+      }
     }
   }
   if (ovf) atomicOr(err, 4);
