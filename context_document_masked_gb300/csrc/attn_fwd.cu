@@ -17,12 +17,12 @@
 // useful (q, k) pairs are visited; tiles on the diagonal or at a segment end
 // are masked element by element.
 //
-// CTA roles (384 threads, persistent over the work list):
+// CTA roles (320 threads, persistent over the work list):
 //   warp 0      TMA producer: Q tiles of both heads, then K/V tiles into a
 //               ring of shared-memory stages.
 //   warp 1      MMA issuer (one thread): S_i = Q_i K^T and O_i += P_i V with
 //               tcgen05.mma, accumulators in TMEM; allocates TMEM.
-//   warps 4-7   softmax for head 0 of the pair, warps 8-11 for head 1: read
+//   warps 2-5   softmax for head 0 of the pair, warps 6-9 for head 1: read
 //               S from TMEM (one row per thread), mask, update the running
 //               max / sum, write P (fp16) back into TMEM over S, rescale O in
 //               TMEM when the max grows by more than 2^8, and finish the rows.
@@ -47,7 +47,7 @@ using namespace dev;
 
 namespace {
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 320;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when the max grows by > 2^8
 
 template <int D>
@@ -316,10 +316,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(&bar_drain);
       mbar_drain(&bar_drain, 0);
     }
-  } else if (warp >= 4) {
+  } else {
     // ------------------------------------------------------------ softmax
-    const int i = (warp - 4) >> 2;          // which head of the pair
-    const int r = tid - 128 * (1 + i);      // tile row == TMEM lane
+    // A warp reaches TMEM lanes 32 * (warp % 4) and up: warps 2-5 (and 6-9)
+    // cover the four lane quarters of one head's tile.
+    const int i = (warp - 2) >> 2;          // which head of the pair
+    const int r = 32 * (warp & 3) + lane;   // tile row == TMEM lane
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const uint32_t s_col = lane_base + C::kColS + i * 128;
     const uint32_t o_col = lane_base + C::kColO + i * D;
@@ -358,15 +360,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < 128; ++c)
               if (c >= lim) s[c] = -INFINITY;
           }
-          // Row max with eight independent chains (one warp per scheduler: keep
-          // the dependent-latency chains short).
+          // Row max: eight independent chains of three-input maxima (one warp
+          // per scheduler: keep the dependent-latency chains short).
           float mx8[8];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) mx8[j] = s[j];
+          for (int j = 0; j < 8; ++j) {
+            float m = fmaxf(s[j], s[j + 8]);
 #pragma unroll
-          for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
-          const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                 fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
+            for (int c = j + 16; c < 128; c += 16) m = fmax3(m, s[c], s[c + 8]);
+            mx8[j] = m;
+          }
+          const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], fmax3(mx8[5], mx8[6], mx8[7]))) *
                            p.scale_log2;
           const float m_new = fmaxf(m_run, mx);
           const bool rescale = m_new > m_run + kRescaleThreshold;
@@ -377,21 +381,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const float m_use = m_run == -INFINITY ? 0.f : m_run;
           // P = exp2(s * scale * log2e - m): fp16 pairs straight into TMEM columns
-          // [0, 64) of S_i, 64 score columns at a time.
-          float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          // [0, 64) of S_i, 64 score columns at a time. The scaling and the row
+          // sum run on packed pairs; sums of column c go to accumulator c mod 8.
+          const uint64_t c2 = f2(p.scale_log2, p.scale_log2), nm2 = f2(-m_use, -m_use);
+          uint64_t rs2[4] = {0, 0, 0, 0};
 #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) {
             float pk[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-              const float p0 = ex2(fmaf(s[64 * h2 + 2 * j], p.scale_log2, -m_use));
-              const float p1 = ex2(fmaf(s[64 * h2 + 2 * j + 1], p.scale_log2, -m_use));
-              rs[(2 * j) & 7] += p0;
-              rs[(2 * j + 1) & 7] += p1;
+              float x0, x1;
+              f2_split(f2_fma(f2(s[64 * h2 + 2 * j], s[64 * h2 + 2 * j + 1]), c2, nm2), x0, x1);
+              const float p0 = ex2(x0), p1 = ex2(x1);
+              rs2[j & 3] = f2_add(rs2[j & 3], f2(p0, p1));
               pk[j] = __uint_as_float(pack_f16(p0, p1));
             }
             tmem_st32(s_col + 32 * h2, pk);
           }
+          float rs[8];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) f2_split(rs2[j], rs[2 * j], rs[2 * j + 1]);
           const float rowsum = ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
           // P_i(t-1) V has completed (see above), so O_i can be rescaled now.
           if (t > 0 && __any_sync(0xffffffffu, rescale)) {
