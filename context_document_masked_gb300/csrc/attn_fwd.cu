@@ -386,17 +386,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t c2 = f2(p.scale_log2, p.scale_log2), nm2 = f2(-m_use, -m_use);
           uint64_t rs2[4] = {0, 0, 0, 0};
 #pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            float pk[32];
+          for (int q4 = 0; q4 < 4; ++q4) {  // 32 score columns -> 16 TMEM columns of P
+            uint32_t pk[16];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
+            for (int j = 0; j < 16; ++j) {
+              const int c = 32 * q4 + 2 * j;
               float x0, x1;
-              f2_split(f2_fma(f2(s[64 * h2 + 2 * j], s[64 * h2 + 2 * j + 1]), c2, nm2), x0, x1);
+              f2_split(f2_fma(f2(s[c], s[c + 1]), c2, nm2), x0, x1);
               const float p0 = ex2(x0), p1 = ex2(x1);
               rs2[j & 3] = f2_add(rs2[j & 3], f2(p0, p1));
-              pk[j] = __uint_as_float(pack_f16(p0, p1));
+              pk[j] = pack_f16(p0, p1);
             }
-            tmem_st32(s_col + 32 * h2, pk);
+            tmem_st16(s_col + 16 * q4, pk);
           }
           float rs[8];
 #pragma unroll
