@@ -213,10 +213,13 @@ int fcp_plan_upload(const fcp_plan_t* plan, void* dev_buf, int64_t bytes, void* 
   return FCP_OK;
 }
 
-// Workspace layout (each region 256-byte aligned): [0, 256) error word; D_i
+// Workspace layout (each region 256-byte aligned): [0, 256) error word (byte
+// 0) and the persistent kernels' work counter (byte kWorkCounterOff); D_i
 // (fp32 [Hq][T]); fp16 copies of Q and dO ([T][Hq][d] each, backward); fp16
 // copies of V ([T][Hkv][d]) and of the received V rows ([R][Hkv][d], R = all
 // shards' remote rows of the plan), the forward's P*V operands.
+constexpr int64_t kWorkCounterOff = 64;
+
 struct WsLayout {
   int64_t delta, q16, do16, v16, vb16, total;
 };
@@ -285,10 +288,12 @@ int fcp_attn_fwd(const void* q, const void* k, const void* v, const void* kbuf, 
   char* wsb = static_cast<char*>(ws);
   void* v16 = wsb + wl.v16;
   void* vb16 = wsb + wl.vb16;
+  int* counter = reinterpret_cast<int*>(wsb + kWorkCounterOff);
   int st2 = fcp::launch_convert_f16(v, v16, (int64_t)dims.T * dims.hkv * dims.d, static_cast<int*>(ws),
-                                    num_sms(), cs);
+                                    counter, num_sms(), cs);
   if (st2 == FCP_OK && rrows > 0)
-    st2 = fcp::launch_convert_f16(vbuf, vb16, rrows * dims.hkv * dims.d, static_cast<int*>(ws), num_sms(), cs);
+    st2 = fcp::launch_convert_f16(vbuf, vb16, rrows * dims.hkv * dims.d, static_cast<int*>(ws), nullptr,
+                                  num_sms(), cs);
   if (st2) return st2;
 
   fcp::FwdLaunch a;
@@ -325,6 +330,7 @@ int fcp_attn_fwd(const void* q, const void* k, const void* v, const void* kbuf, 
   fp.out = out;
   fp.lse = lse;
   fp.err = static_cast<int*>(ws);
+  fp.work_counter = counter;
   fp.wait_ns = g_wait_ns;
   a.d = dims.d;
   a.num_sms = num_sms();
@@ -374,7 +380,8 @@ int fcp_attn_bwd(const void* q, const void* k, const void* v, const void* kbuf, 
   }
   st = fcp::launch_bwd_preprocess(out, out_dtype == FCP_OUT_F32, dout, q, table(plan, fcp::TB_ROWS),
                                   table(plan, fcp::TB_IDENT) + r0, r1 - r0, dims.T, dims.hq, dims.d,
-                                  delta, dq, q16, do16, static_cast<int*>(ws), s);
+                                  delta, dq, q16, do16, static_cast<int*>(ws),
+                                  reinterpret_cast<int*>(wsb + kWorkCounterOff), s);
   if (st) return st;
 
   fcp::BwdLaunch a;
@@ -413,6 +420,7 @@ int fcp_attn_bwd(const void* q, const void* k, const void* v, const void* kbuf, 
   bp.dk = dk;
   bp.dv = dv;
   bp.err = static_cast<int*>(ws);
+  bp.work_counter = reinterpret_cast<int*>(wsb + kWorkCounterOff);
   bp.wait_ns = g_wait_ns;
   a.d = dims.d;
   a.num_sms = num_sms();

@@ -142,6 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t bar_q_full[2], bar_q_empty[2], bar_do_full, bar_do_empty;
   __shared__ __align__(8) uint64_t bar_s_full, bar_dp_full, bar_p_ready, bar_ds_ready, bar_ds_free;
   __shared__ __align__(8) uint64_t bar_dq_full, bar_dq_free, bar_dkdv_full, bar_dkdv_free;
+  __shared__ WorkRing<4> ring;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
@@ -170,6 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bar_dq_free, 128);
     mbar_init(&bar_dkdv_full, 1);
     mbar_init(&bar_dkdv_free, 256);
+    ring.init(1 + 2 + 8 + 4);  // MMA thread, conversion, compute and dQ warps
     abort_sh = 0;
     fence_barrier_init();
   }
@@ -201,7 +203,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t issued_q[2] = {0, 0};
     bool ok = true;
     const float kLog2e = 1.4426950408889634f;
-    for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
+    uint32_t k = 0;
+    for (int w = blockIdx.x; ok;) {
+      if (lane == 0) ok = ring.put(k, w, wc);
+      ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
+      ++k;
+      if (!ok || w >= n_work) break;
+      // The next unit is claimed now, so its tiles can be prefetched into L2.
+      int w_next = 0;
+      if (lane == 0) w_next = next_work(p.work_counter);
+      w_next = __shfl_sync(0xffffffffu, w_next, 0);
       const BwdItem it = decode(p, w);
       if (kv_items > 0) {
         ok = mbar_wait(&bar_kv_empty, (kv_items - 1) & 1, wc);
@@ -220,8 +231,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nsteps = G * it.n_qt;
       // L2 prefetches: the next unit's K/V tiles now, each step's Q/dO tiles
       // two steps ahead, so the shared-memory loads above hit in L2.
-      if (lane == 0 && w + (int)gridDim.x < n_work) {
-        const BwdItem nx = decode(p, w + gridDim.x);
+      if (lane == 0 && w_next < n_work) {
+        const BwdItem nx = decode(p, w_next);
         for (int pn = 0; pn < C::kPanels; ++pn) {
           tma_prefetch_3d(nx.src ? &tm_kb : &tm_k, pn * 64, nx.g, nx.src_row);
           tma_prefetch_3d(nx.src ? &tm_vb : &tm_v, pn * 64, nx.g, nx.src_row);
@@ -274,6 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++dc;
       }
+      w = w_next;
     }
     if (lane == 0) {  // every copy this warp started has landed before the CTA exits
       if (kv_items) mbar_drain(&bar_kv_full, (kv_items - 1) & 1);
@@ -311,7 +323,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(&bar_dp_full);
       };
-      for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
+      for (uint32_t k = 0; ok; ++k) {
+        int w;
+        if (!(ok = ring.get(k, w, wc))) break;
+        ring.release(k);
+        if (w >= n_work) break;
         const BwdItem it = decode(p, w);
         const int nsteps = G * it.n_qt;
         if (!(ok = mbar_wait(&bar_kv_conv, kv_items & 1, wc))) break;
@@ -381,7 +397,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t items = 0;
     bool ok = true, ovf = false;
     uint4* kv = reinterpret_cast<uint4*>(smem + C::kK);  // K and V tiles are contiguous
-    for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
+    for (uint32_t k = 0; ok; ++k) {
+      int w = 0;
+      ok = ring.get(k, w, wc);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      __syncwarp();
+      if (lane == 0) ring.release(k);
+      if (w >= n_work) break;
       ok = mbar_wait(&bar_kv_full, items & 1, wc);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
 #pragma unroll 4
@@ -408,7 +430,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t ds_panel = smem_u32(smem + C::kDS) + half * 16384;
     uint32_t qc = 0, gstep = 0, items = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
+    for (uint32_t k = 0; ok; ++k) {
+      int w = 0;
+      ok = ring.get(k, w, wc);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      __syncwarp();
+      if (lane == 0) ring.release(k);
+      if (w >= n_work) break;
       const BwdItem it = decode(p, w);
       const int nsteps = G * it.n_qt;
       const bool key_valid = kr < it.n;
@@ -527,7 +555,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* stage = smem + C::kStage;
     uint32_t gstep = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
+    for (uint32_t k = 0; ok; ++k) {
+      int w = 0;
+      ok = drain_group_all(ring.get(k, w, wc));
+      if (!ok) break;
+      __syncwarp();
+      if (lane == 0) ring.release(k);
+      if (w >= n_work) break;
       const BwdItem it = decode(p, w);
       const int nsteps = G * it.n_qt;
       for (int j = 0; j < nsteps; ++j, ++gstep) {

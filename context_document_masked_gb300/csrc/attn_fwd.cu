@@ -152,6 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t bar_q_full, bar_q_empty, bar_drain;
   __shared__ __align__(8) uint64_t bar_kv_full[C::kStages], bar_kv_empty[C::kStages];
   __shared__ __align__(8) uint64_t bar_s_full[2], bar_p_ready[2], bar_o_done[2], bar_o_free[2];
+  __shared__ WorkRing<4> ring;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
@@ -173,6 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar_o_done[i], 1);
       mbar_init(&bar_o_free[i], 128);
     }
+    ring.init(1 + 8);  // the MMA thread and the eight softmax warps
     abort_sh = 0;
     fence_barrier_init();
   }
@@ -204,12 +206,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t issued[C::kStages];
       for (int s = 0; s < C::kStages; ++s) issued[s] = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
+      uint32_t k = 0;
+      for (int w = blockIdx.x; ok; w = next_work(p.work_counter)) {
+        if (!(ok = ring.put<true>(k++, w, wc)) || w >= n_work) break;
         const WorkItem it = decode(p, w);
         const int q_last = it.q_start + it.q_rows - 1;
         const int nt = count_key_tiles(p.segs, it.seg_begin, it.seg_count, q_last, p.kv_lo, p.kv_hi);
         if (nt == 0) continue;
-        if (q_iter > 0 && !(ok = mbar_wait(&bar_q_empty, (q_iter - 1) & 1, wc))) break;
+        if (q_iter > 0 && !(ok = mbar_wait_inline(&bar_q_empty, (q_iter - 1) & 1, wc))) break;
         mbar_arrive_expect_tx(&bar_q_full, 2 * C::kTileBytes);
         for (int h = 0; h < 2; ++h)
           for (int pn = 0; pn < C::kPanels; ++pn)
@@ -223,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kv = 0; kv < 2; ++kv) {
             const int s = kv_cnt % C::kStages;
             if (kv_cnt >= (uint32_t)C::kStages &&
-                !(ok = mbar_wait(&bar_kv_empty[s], ((kv_cnt / C::kStages) - 1) & 1, wc)))
+                !(ok = mbar_wait_inline(&bar_kv_empty[s], ((kv_cnt / C::kStages) - 1) & 1, wc)))
               break;
             mbar_arrive_expect_tx(&bar_kv_full[s], C::kTileBytes);
             const CUtensorMap* tm = kv == 0 ? (src ? &tm_kb : &tm_k) : (src ? &tm_vb : &tm_v);
@@ -267,17 +271,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_f16_ts(tmem + C::kColO + i * D, tmem + C::kColS + i * 128 + kk * 8,
                      smem_desc_sw128(va + kk * 2048, 16384, 1024), idesc_o, (acc || kk > 0));
       };
-      for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
+      for (uint32_t k = 0; ok; ++k) {
+        int w;
+        if (!(ok = ring.get<true>(k, w, wc))) break;
+        ring.release(k);
+        if (w >= n_work) break;
         const WorkItem it = decode(p, w);
         const int q_last = it.q_start + it.q_rows - 1;
         const int nt = count_key_tiles(p.segs, it.seg_begin, it.seg_count, q_last, p.kv_lo, p.kv_hi);
         if (nt == 0) continue;
-        if (!(ok = mbar_wait(&bar_q_full, q_iter & 1, wc))) break;
+        if (!(ok = mbar_wait_inline(&bar_q_full, q_iter & 1, wc))) break;
         tc_fence_after();
         // S_0, S_1 of the first key tile.
         {
           const uint32_t c = kv_cnt, s = c % C::kStages;
-          if (!(ok = mbar_wait(&bar_kv_full[s], (c / C::kStages) & 1, wc))) break;
+          if (!(ok = mbar_wait_inline(&bar_kv_full[s], (c / C::kStages) & 1, wc))) break;
           tc_fence_after();
           issue_s(0, s);
           mma_commit(&bar_s_full[0]);
@@ -287,18 +295,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int t = 0; t < nt && ok; ++t) {
           const uint32_t cv = kv_cnt + 2 * t + 1, sv = cv % C::kStages;
-          if (!(ok = mbar_wait(&bar_kv_full[sv], (cv / C::kStages) & 1, wc))) break;
+          if (!(ok = mbar_wait_inline(&bar_kv_full[sv], (cv / C::kStages) & 1, wc))) break;
           for (int i = 0; i < 2; ++i) {
-            if (!(ok = mbar_wait(&bar_p_ready[i], p_cnt[i] & 1, wc))) break;
+            if (!(ok = mbar_wait_inline(&bar_p_ready[i], p_cnt[i] & 1, wc))) break;
             ++p_cnt[i];
-            if (t == 0 && items > 0 && !(ok = mbar_wait(&bar_o_free[i], (items - 1) & 1, wc))) break;
+            if (t == 0 && items > 0 && !(ok = mbar_wait_inline(&bar_o_free[i], (items - 1) & 1, wc))) break;
             tc_fence_after();
             issue_o(i, sv, t > 0);
             if (t + 1 == nt) mma_commit(&bar_o_done[i]);  // O_i final: the epilogue may read it
             if (i == 1) mma_commit(&bar_kv_empty[sv]);
             if (t + 1 < nt) {
               const uint32_t ck = kv_cnt + 2 * (t + 1), sk = ck % C::kStages;
-              if (!(ok = mbar_wait(&bar_kv_full[sk], (ck / C::kStages) & 1, wc))) break;
+              if (!(ok = mbar_wait_inline(&bar_kv_full[sk], (ck / C::kStages) & 1, wc))) break;
               tc_fence_after();
               issue_s(i, sk);
               mma_commit(&bar_s_full[i]);
@@ -327,7 +335,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t o_col = lane_base + C::kColO + i * D;
     uint32_t s_cnt = 0, o_cnt = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < n_work && ok; w += gridDim.x) {
+    for (uint32_t k = 0; ok; ++k) {
+      int w = 0;
+      ok = ring.get<true>(k, w, wc);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      __syncwarp();
+      if (lane == 0) ring.release(k);
+      if (w >= n_work) break;
       const WorkItem it = decode(p, w);
       const int q_last = it.q_start + it.q_rows - 1;
       const int nt = count_key_tiles(p.segs, it.seg_begin, it.seg_count, q_last, p.kv_lo, p.kv_hi);
@@ -341,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int src, row, key, n;
         for (int t = 0; t < nt; ++t) {
           wk.next(src, row, key, n);
-          ok = mbar_wait(&bar_s_full[i], s_cnt & 1, wc);
+          ok = mbar_wait_inline(&bar_s_full[i], s_cnt & 1, wc);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           ++s_cnt;
           tc_fence_after();
@@ -421,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&bar_p_ready[i]);
         }
         if (!ok) break;
-        ok = mbar_wait(&bar_o_done[i], o_cnt & 1, wc);
+        ok = mbar_wait_inline(&bar_o_done[i], o_cnt & 1, wc);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         ++o_cnt;
         tc_fence_after();

@@ -174,7 +174,8 @@ __global__ void __launch_bounds__(kPreThreads)
                       const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ rows,
                       const int32_t* __restrict__ order, int n_chunks, int T, int hq,
                       float* __restrict__ delta, float* __restrict__ dq, __half* __restrict__ q16,
-                      __half* __restrict__ do16, int* __restrict__ err) {
+                      __half* __restrict__ do16, int* __restrict__ err, int* __restrict__ zero_word) {
+  if (zero_word && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *zero_word = 0;
   // A chunk's rows, all heads, are one contiguous [rows][hq][D] block. Each
   // thread takes 8 consecutive elements (16-byte loads of dO and Q, 16 or 32
   // bytes of O); L = D / 8 lanes hold one (row, head) and reduce its D_i.
@@ -246,7 +247,9 @@ __global__ void __launch_bounds__(kPreThreads)
 constexpr int kCvtThreads = 256;
 
 __global__ void __launch_bounds__(kCvtThreads)
-    convert_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t n, int* err) {
+    convert_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t n, int* err,
+                   int* zero_word) {
+  if (zero_word && blockIdx.x == 0 && threadIdx.x == 0) *zero_word = 0;
   bool ovf = false;
   for (int64_t i = (int64_t)blockIdx.x * kCvtThreads + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * kCvtThreads) {
@@ -262,14 +265,15 @@ __global__ void __launch_bounds__(kCvtThreads)
 
 }  // namespace
 
-int launch_convert_f16(const void* src, void* dst, int64_t n_elems, int* err, int num_sms,
-                       cudaStream_t st) {
+int launch_convert_f16(const void* src, void* dst, int64_t n_elems, int* err, int* zero_word,
+                       int num_sms, cudaStream_t st) {
   const int64_t n = n_elems / 8;
-  if (n == 0) return FCP_OK;
+  if (n == 0 && !zero_word) return FCP_OK;
   int64_t grid = (n + kCvtThreads - 1) / kCvtThreads;
   if (grid > (int64_t)num_sms * 16) grid = (int64_t)num_sms * 16;
+  if (grid < 1) grid = 1;
   convert_kernel<<<(int)grid, kCvtThreads, 0, st>>>(static_cast<const uint4*>(src),
-                                                    static_cast<uint4*>(dst), n, err);
+                                                    static_cast<uint4*>(dst), n, err, zero_word);
   return cudaGetLastError() == cudaSuccess ? FCP_OK : FCP_ERR_CUDA;
 }
 
@@ -322,14 +326,15 @@ int launch_merge(const float* o_parts, const float* lse_parts, int32_t B, int64_
 int launch_bwd_preprocess(const void* out, bool out_f32, const void* dout, const void* q,
                           const int32_t* rows, const int32_t* order, int32_t n_chunks, int32_t T,
                           int32_t hq, int32_t d, float* delta, float* dq, void* q16, void* do16,
-                          int* err, cudaStream_t st) {
-  if (n_chunks == 0) return FCP_OK;
-  const dim3 grid(n_chunks, 8);  // a chunk's (row, head) pairs spread over 8 blocks
+                          int* err, int* zero_word, cudaStream_t st) {
+  if (n_chunks == 0 && !zero_word) return FCP_OK;
+  const dim3 grid(n_chunks > 0 ? n_chunks : 1, 8);  // a chunk's (row, head) pairs over 8 blocks
   using B = __nv_bfloat16;
   auto go = [&](auto kernel) {
     kernel<<<grid, kPreThreads, 0, st>>>(out, static_cast<const B*>(dout), static_cast<const B*>(q),
                                          rows, order, n_chunks, T, hq, delta, dq,
-                                         static_cast<__half*>(q16), static_cast<__half*>(do16), err);
+                                         static_cast<__half*>(q16), static_cast<__half*>(do16), err,
+                                         zero_word);
   };
   if (d == 128)
     out_f32 ? go(preprocess_kernel<128, true>) : go(preprocess_kernel<128, false>);

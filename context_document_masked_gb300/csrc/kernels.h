@@ -23,6 +23,7 @@ struct FwdParams {
   void* out;
   float* lse;
   int* err;
+  int* work_counter;       // zero at launch (set by the preceding kernel of the call)
   int64_t wait_ns;
 };
 
@@ -48,6 +49,7 @@ struct BwdParams {
   float* dk;               // [T][Hkv][d] fp32, accumulated
   float* dv;
   int* err;
+  int* work_counter;       // zero at launch (set by the preprocess)
   int64_t wait_ns;
 };
 
@@ -64,14 +66,18 @@ int launch_attn_bwd(const BwdLaunch& a, cudaStream_t st);
 
 // Row statistics D_i = <dO_i, O_i> for the rows of the given row chunks, dQ
 // rows set to zero, and fp16 copies of Q and dO for the backward's MMAs.
+// *zero_word (if not null) is set to 0: the work counter of the kernel that
+// follows in the same stream.
 int launch_bwd_preprocess(const void* out, bool out_f32, const void* dout, const void* q,
                           const int32_t* rows,
                           const int32_t* order, int32_t n_chunks, int32_t T, int32_t hq, int32_t d,
-                          float* delta, float* dq, void* q16, void* do16, int* err, cudaStream_t st);
+                          float* delta, float* dq, void* q16, void* do16, int* err, int* zero_word,
+                          cudaStream_t st);
 
-// fp16 copy of a bf16 array of n_elems (a multiple of 8) elements.
-int launch_convert_f16(const void* src, void* dst, int64_t n_elems, int* err, int num_sms,
-                       cudaStream_t st);
+// fp16 copy of a bf16 array of n_elems (a multiple of 8) elements; *zero_word
+// (if not null) is set to 0, as above.
+int launch_convert_f16(const void* src, void* dst, int64_t n_elems, int* err, int* zero_word,
+                       int num_sms, cudaStream_t st);
 
 // Gather of received KV rows: tasks (src_row, dst_row, nrows, shard).
 int launch_gather(const void* k, const void* v, const int32_t* tasks, int32_t n_tasks,

@@ -111,7 +111,9 @@ extern "C" int fcp_attn_fwd_noalloc(const void* q, const void* k, const void* v,
     if (!aligned16(ptr)) return FCP_ERR_INVALID_ARG;
   if (rrows > 0 && (!aligned16(kbuf) || !aligned16(vbuf))) return FCP_ERR_INVALID_ARG;
 
-  // Scratch layout: error word, fp16 V [T][Hkv][d], fp16 received V [rrows][Hkv][d].
+  // Scratch layout: error word (byte 0) and the forward kernel's work counter
+  // (byte 64) in the first 256 bytes, fp16 V [T][Hkv][d], fp16 received V
+  // [rrows][Hkv][d].
   const int64_t v16_off = 256;
   const int64_t vb16_off = v16_off + align256((int64_t)dims.T * dims.hkv * dims.d * 2);
   const int64_t need = vb16_off + align256(rrows * dims.hkv * dims.d * 2);
@@ -126,9 +128,10 @@ extern "C" int fcp_attn_fwd_noalloc(const void* q, const void* k, const void* v,
   void* vb16 = base + vb16_off;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(err, 0, sizeof(int), cs) != cudaSuccess) return FCP_ERR_CUDA;
-  st = fcp::launch_convert_f16(v, v16, (int64_t)dims.T * dims.hkv * dims.d, err, num_sms(), cs);
+  int* counter = reinterpret_cast<int*>(base + 64);  // the forward kernel's work counter
+  st = fcp::launch_convert_f16(v, v16, (int64_t)dims.T * dims.hkv * dims.d, err, counter, num_sms(), cs);
   if (st == FCP_OK && rrows > 0)
-    st = fcp::launch_convert_f16(vbuf, vb16, rrows * dims.hkv * dims.d, err, num_sms(), cs);
+    st = fcp::launch_convert_f16(vbuf, vb16, rrows * dims.hkv * dims.d, err, nullptr, num_sms(), cs);
   if (st) return st;
 
   fcp::FwdLaunch a;
@@ -170,6 +173,7 @@ extern "C" int fcp_attn_fwd_noalloc(const void* q, const void* k, const void* v,
   fp.out = out;
   fp.lse = lse;
   fp.err = err;
+  fp.work_counter = counter;
   fp.wait_ns = 2000000000LL;
   a.d = dims.d;
   a.num_sms = num_sms();

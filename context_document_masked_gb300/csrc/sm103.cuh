@@ -61,10 +61,8 @@ struct WaitCtl {
 
 enum : int { kErrTimeout = 1 };
 
-// Bounded wait for phase `parity` of `bar`. Returns false if the wait gave up
-// (deadline passed, or another role of the CTA aborted). Never traps.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Deadline loop of a bounded wait.
+__device__ __forceinline__ bool mbar_wait_loop(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
   if (w.limit_ns < 0) {
     *w.abort_flag = 1;
     atomicOr(w.err, kErrTimeout);
@@ -83,6 +81,26 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   }
 }
 
+// The loop kept out of line: a kernel with many wait sites (the backward)
+// would otherwise crowd the instruction cache of its hot loops.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
+  return mbar_wait_loop(bar, parity, w);
+}
+
+// Bounded wait for phase `parity` of `bar`. Returns false if the wait gave up
+// (deadline passed, or another role of the CTA aborted). Never traps.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, w);
+}
+
+// The same with the loop inlined (no call: for kernels with few wait sites and
+// no registers to spare around a call).
+__device__ __forceinline__ bool mbar_wait_inline(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_loop(bar, parity, w);
+}
+
 // Wait used while tearing down after an abort: fixed limit, no abort check.
 __device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = globaltimer();
@@ -91,6 +109,52 @@ __device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity) {
   }
   return true;
 }
+
+// --------------------------------------------------------- work sequence
+// Dynamic work distribution inside a persistent CTA. One producer thread
+// draws work indices (its first is blockIdx.x, the rest come from a global
+// counter that starts at zero) and publishes them in order through a ring of
+// shared-memory slots; every other role of the CTA reads the same sequence.
+// An index >= the work count ends it. A CTA that finishes early takes the
+// next unclaimed unit, so no CTA is left holding a static share of long units.
+template <int R>
+struct WorkRing {
+  int slot[R];
+  uint64_t full[R];
+  uint64_t empty[R];
+
+  __device__ void init(uint32_t consumers) {
+    for (int r = 0; r < R; ++r) {
+      mbar_init(&full[r], 1);
+      mbar_init(&empty[r], consumers);
+    }
+  }
+  // Producer: entry k of the sequence is w (waits until slot k % R is free).
+  template <bool kInline = false>
+  __device__ bool put(uint32_t k, int w, const WaitCtl& wc) {
+    const uint32_t r = k % R;
+    if (k >= (uint32_t)R &&
+        !(kInline ? mbar_wait_inline(&empty[r], ((k / R) - 1) & 1, wc) : mbar_wait(&empty[r], ((k / R) - 1) & 1, wc)))
+      return false;
+    *reinterpret_cast<volatile int*>(&slot[r]) = w;
+    mbar_arrive(&full[r]);  // release: the slot write is visible to the waiters
+    return true;
+  }
+  // Consumer: entry k of the sequence.
+  template <bool kInline = false>
+  __device__ bool get(uint32_t k, int& w, const WaitCtl& wc) {
+    const uint32_t r = k % R;
+    if (!(kInline ? mbar_wait_inline(&full[r], (k / R) & 1, wc) : mbar_wait(&full[r], (k / R) & 1, wc)))
+      return false;
+    w = *reinterpret_cast<volatile int*>(&slot[r]);
+    return true;
+  }
+  // Consumer (one arrival per consumer of the init count): done with entry k.
+  __device__ void release(uint32_t k) { mbar_arrive(&empty[k % R]); }
+};
+
+// Next work index for this CTA after its first (blockIdx.x).
+__device__ __forceinline__ int next_work(int* counter) { return (int)gridDim.x + atomicAdd(counter, 1); }
 
 // --------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, uint64_t* bar, int c0,
