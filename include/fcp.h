@@ -180,10 +180,13 @@ typedef struct {
   float scale;    /* softmax scale; 0 selects 1/sqrt(d)                */
 } fcp_dims;
 
-/* Workspace the device calls on `plan` need, in bytes: an error word, the
+/* Workspace the device calls on `plan` need, in bytes: an error word and the
+ * attention kernels' work counter (set by each call before use), the
  * backward's row statistics D_i = <dO_i, O_i> ([Hq][T] fp32), fp16 copies of
  * Q and dO ([T][Hq][d] each, the backward's tensor-core operands) and of V and
- * the plan's received V rows (the forward's P*V operands). */
+ * the plan's received V rows (the forward's P*V operands). Calls that share a
+ * workspace must be ordered on the GPU (one stream, or synchronised): two at
+ * once would race on these contents. */
 int64_t fcp_workspace_bytes(fcp_dims dims, const fcp_plan_t* plan);
 
 /*
@@ -265,8 +268,8 @@ int fcp_attn_bwd(const void* q, const void* k, const void* v, const void* kbuf,
  * where a cudaMalloc would synchronise the device and can fail once memory is
  * fragmented.
  *   Arguments, layouts and results are those of fcp_attn_fwd, minus ws and
- *   ws_bytes. The scratch (an error word and fp16 copies of V and of the
- *   received V rows) is one file-scope device array of
+ *   ws_bytes. The scratch (an error word, the kernel's work counter and fp16
+ *   copies of V and of the received V rows) is one file-scope device array of
  *   FCP_NOALLOC_SCRATCH_BYTES bytes, held by every GPU that loads the library
  *   until the process exits.
  *   Limit: 256 + align256(T*Hkv*d*2) + align256(R*Hkv*d*2) bytes must fit in
