@@ -33,6 +33,32 @@ METRIC = "doc-masked attn useful TFLOPS fwd+bwd (% of GB300 BF16 peak); merge GB
 UNIT = "TFLOP/s"
 
 
+# DRAM bytes of one backward call (preprocess + main kernel) on this workload,
+# from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum of both
+# kernels; profiles/attn_fwd_bwd_packed32k_h32kv8_d128_cp4_perdoc.md and
+# profiles/bandwidth_kernels_packed32k.md). Valid only for the sources it was
+# taken on: reported as null once any of them changes.
+BWD_TRAFFIC = {
+    "sources": ["context_document_masked_gb300/csrc/attn_bwd.cu", "context_document_masked_gb300/csrc/copy_kernels.cu",
+                "context_document_masked_gb300/csrc/sm103.cuh", "context_document_masked_gb300/csrc/kernels.h",
+                "context_document_masked_gb300/csrc/api.cu"],
+    "sha256": "f43f06851e21ef4192066b0687b75bce19ec1ed8d81c3951b6880f28e6900d18",
+    "bytes": (2.741944 + 1.447788 + 1.087363 + 1.043690) * 1e9,
+}
+
+
+def _bwd_traffic():
+    import hashlib
+    h = hashlib.sha256()
+    try:
+        for f in BWD_TRAFFIC["sources"]:
+            with open(os.path.join(ROOT, f), "rb") as fh:
+                h.update(fh.read())
+    except OSError:
+        return None
+    return BWD_TRAFFIC["bytes"] if h.hexdigest() == BWD_TRAFFIC["sha256"] else None
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -231,7 +257,8 @@ def run_gpu(args):
         "roofline": {"bound": "tensor", "kernel": "fcp_attn_bwd (preprocess + main)", "achieved": round(bwd_ach, 2),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(bwd_ach / peak, 4),
                      "peak_note": f"{pk['source']} bf16 sustained; fp16 MMA has the same nominal rate",
-                     "traffic": None},
+                     "traffic": _bwd_traffic(), "traffic_unit": "bytes per call (DRAM read + write, ncu)",
+                     "algorithmic": "10*d*Hq*P flops per call, P = useful (q, k) pairs per head"},
         "kernels_ms": {k_: round(v_, 4) for k_, v_ in per.items()},
         "fwd": {"tflops": round(fwd_flops / (per["fwd"] * 1e-3) / 1e12, 2),
                 "frac": round(fwd_flops / (per["fwd"] * 1e-3) / 1e12 / peak, 4)},
