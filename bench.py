@@ -150,6 +150,24 @@ def _dist():
     return ws, rank
 
 
+def _max_over_ranks(value: float, dist, device) -> float:
+    """The slowest rank's time: every rank contributes its own and all get the max."""
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _job_tflops(world: int, flops_per_replica: float, ms_step: float) -> float:
+    """Whole-job throughput: every rank runs one replica of the workload per
+    step (weak scaling), timed by the slowest rank."""
+    return world * flops_per_replica / (ms_step * 1e-3) / 1e12
+
+
+def _replica_seed(rank: int) -> int:
+    return 1000 + CFG + rank
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -165,7 +183,7 @@ def run_gpu(args):
         dist.init_process_group("nccl")
     w, D, pairs = _workload()
     T, hq, hkv, d = w.T, w.Hq, w.Hkv, w.d
-    seed = 1000 + CFG + rank          # independent replica per rank
+    seed = _replica_seed(rank)        # independent replica per rank
     q, k, v = synth.make_qkv(T, hq, hkv, d, seed=seed, device=dev)
     do = synth.make_dout(T, hq, d, seed=seed, device=dev)
     s = CPAttention(D, w.cp, w.policy, hq, hkv, d, device=dev)
@@ -211,15 +229,13 @@ def run_gpu(args):
         dist.barrier()
     ms_total = t_start.elapsed_time(t_end)
     if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+        ms_total = _max_over_ranks(ms_total, dist, dev)
     ms_step = ms_total / args.steps
     per = {n: statistics.mean(ev[a][i].elapsed_time(ev[b][i]) for i in range(args.steps))
            for n, a, b in (("gather", "gather", "fwd"), ("fwd", "fwd", "bwd"), ("bwd", "bwd", "end"))}
     fwd_flops = 4.0 * d * hq * pairs
     bwd_flops = 10.0 * d * hq * pairs
-    value = world * (fwd_flops + bwd_flops) / (ms_step * 1e-3) / 1e12
+    value = _job_tflops(world, fwd_flops + bwd_flops, ms_step)
     pk = _peaks()
     stats = s.stats()
     remote_rows = stats["remote_rows_total"]
