@@ -292,6 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_s(1, s);
           mma_commit(&bar_s_full[1]);
           mma_commit(&bar_kv_empty[s]);
+          if (nt == 1) mma_commit(&bar_q_empty);  // no S left to issue: Q may be replaced
         }
         for (int t = 0; t < nt && ok; ++t) {
           const uint32_t cv = kv_cnt + 2 * t + 1, sv = cv % C::kStages;
@@ -311,11 +312,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               issue_s(i, sk);
               mma_commit(&bar_s_full[i]);
               if (i == 1) mma_commit(&bar_kv_empty[sk]);
+              // After the last tile's S of both heads, Q is not read again:
+              // the next unit's Q tiles may load while this unit finishes.
+              if (i == 1 && t + 2 == nt) mma_commit(&bar_q_empty);
             }
           }
         }
         if (!ok) break;
-        mma_commit(&bar_q_empty);
         kv_cnt += 2 * nt;
         ++q_iter;
         ++items;
@@ -335,6 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t o_col = lane_base + C::kColO + i * D;
     uint32_t s_cnt = 0, o_cnt = 0;
     bool ok = true;
+    const bool out_v8 = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
     for (uint32_t k = 0; ok; ++k) {
       int w = 0;
       ok = ring.get<true>(k, w, wc);
@@ -453,21 +457,37 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = 0.f;
         }
+        // A thread writes its own row: 32-byte stores where `out` allows
+        // them (each row segment is then whole sectors), else 16-byte ones.
         if (row_valid) {
           if (p.out_f32) {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + obase + c * 32);
+            float* dst = static_cast<float*>(p.out) + obase + c * 32;
+            if (out_v8) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              dst[j] = make_float4(v[4 * j] * inv, v[4 * j + 1] * inv, v[4 * j + 2] * inv,
-                                   v[4 * j + 3] * inv);
+              for (int j = 0; j < 4; ++j)
+                st_global_v8(dst + 8 * j, __float_as_uint(v[8 * j] * inv), __float_as_uint(v[8 * j + 1] * inv),
+                             __float_as_uint(v[8 * j + 2] * inv), __float_as_uint(v[8 * j + 3] * inv),
+                             __float_as_uint(v[8 * j + 4] * inv), __float_as_uint(v[8 * j + 5] * inv),
+                             __float_as_uint(v[8 * j + 6] * inv), __float_as_uint(v[8 * j + 7] * inv));
+            } else {
+              float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                d4[j] = make_float4(v[4 * j] * inv, v[4 * j + 1] * inv, v[4 * j + 2] * inv, v[4 * j + 3] * inv);
+            }
           } else {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + obase + c * 32);
+            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + obase + c * 32;
+            uint32_t w[16];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              dst[j] = make_uint4(pack_bf16(v[8 * j] * inv, v[8 * j + 1] * inv),
-                                  pack_bf16(v[8 * j + 2] * inv, v[8 * j + 3] * inv),
-                                  pack_bf16(v[8 * j + 4] * inv, v[8 * j + 5] * inv),
-                                  pack_bf16(v[8 * j + 6] * inv, v[8 * j + 7] * inv));
+            for (int j = 0; j < 16; ++j) w[j] = pack_bf16(v[2 * j] * inv, v[2 * j + 1] * inv);
+            if (out_v8) {
+              st_global_v8(dst, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+              st_global_v8(dst + 16, w[8], w[9], w[10], w[11], w[12], w[13], w[14], w[15]);
+            } else {
+              uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) d4[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+            }
           }
         }
       }

@@ -76,6 +76,28 @@ def test_forward_all_shards(cuda, case):
     assert _bf16_excess(out, o_ref) <= TOL_O
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_forward_output_only_16_byte_aligned(cuda, dtype):
+    """The API asks for 16-byte alignment of `out`; the kernel stores 32 bytes
+    at a time only when the pointer allows it. Output written at a 16-byte
+    offset (the narrower stores) equals the aligned output bit for bit."""
+    case = SMALL[3]
+    name, D, hq, hkv, d, cp, pol = case
+    s, cu, q, k, v, qd, kd, vd = _setup(*case)
+    s.gather(kd, vd)
+    ref, lse_ref = s.forward(qd, kd, vd, out_dtype=dtype)
+    shift = 16 // torch.tensor([], dtype=dtype).element_size()
+    flat = torch.full((s.T * hq * d + shift,), float("nan"), dtype=dtype, device=s.device)
+    out = flat[shift:].view(s.T, hq, d)
+    assert out.data_ptr() % 32 == 16
+    lse = torch.empty_like(lse_ref)
+    s.forward(qd, kd, vd, out=out, lse=lse, out_dtype=dtype)
+    torch.cuda.synchronize()
+    assert s.device_status() == 0
+    assert torch.equal(out, ref) and torch.equal(lse, lse_ref)
+    assert torch.isnan(flat[:shift].float()).all()  # nothing written before `out`
+
+
 @pytest.mark.parametrize("case", SMALL[:6], ids=[c[0] for c in SMALL[:6]])
 def test_forward_one_shard_at_a_time(cuda, case):
     """Each shard alone, with only its own received keys gathered: assembling
