@@ -389,7 +389,9 @@ int fcp_attn_bwd(const void* q, const void* k, const void* v, const void* kbuf, 
   bool ok = make_map(&a.tm_q, q16, dims.d, dims.hq, dims.T, true) &&
             make_map(&a.tm_do, do16, dims.d, dims.hq, dims.T, true) &&
             make_map(&a.tm_k, k, dims.d, dims.hkv, dims.T) && make_map(&a.tm_v, v, dims.d, dims.hkv, dims.T) &&
-            make_map_f32(&a.tm_dq, dq, dims.d, dims.hq, dims.T);
+            make_map_f32(&a.tm_dq, dq, dims.d, dims.hq, dims.T) &&
+            make_map_f32(&a.tm_dk, dk, dims.d, dims.hkv, dims.T) &&
+            make_map_f32(&a.tm_dv, dv, dims.d, dims.hkv, dims.T);
   if (rrows > 0)
     ok = ok && make_map(&a.tm_kb, kbuf, dims.d, dims.hkv, rrows) &&
          make_map(&a.tm_vb, vbuf, dims.d, dims.hkv, rrows);

@@ -92,12 +92,6 @@ __device__ __forceinline__ BwdItem decode(const BwdParams& p, int w) {
   return it;
 }
 
-__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
-               "f"(d)
-               : "memory");
-}
-
 // TMA bulk reduce-add of a shared-memory tile into global memory.
 __device__ __forceinline__ void tma_reduce_add_3d(const void* tmap, const void* src, int c0, int c1,
                                                   int c2) {
@@ -135,13 +129,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_kb, const __grid_constant__ CUtensorMap tm_vb,
-                    const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
+                    const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
+                    const __grid_constant__ CUtensorMap tm_dv, const BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ __align__(8) uint64_t bar_kv_full, bar_kv_conv, bar_kv_empty, bar_drain;
   __shared__ __align__(8) uint64_t bar_q_full[2], bar_q_empty[2], bar_do_full, bar_do_empty;
   __shared__ __align__(8) uint64_t bar_s_full, bar_dp_full, bar_p_ready, bar_ds_ready, bar_ds_free;
   __shared__ __align__(8) uint64_t bar_dq_full, bar_dq_free, bar_dkdv_full, bar_dkdv_free;
+  __shared__ __align__(8) uint64_t bar_stg_full[2], bar_stg_free[2];  // dV / dK staging, per half
   __shared__ WorkRing<4> ring;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
@@ -171,6 +167,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bar_dq_free, 128);
     mbar_init(&bar_dkdv_full, 1);
     mbar_init(&bar_dkdv_free, 256);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(&bar_stg_full[h], 128);
+      mbar_init(&bar_stg_free[h], 1);
+    }
     ring.init(1 + 2 + 8 + 4);  // MMA thread, conversion, compute and dQ warps
     abort_sh = 0;
     fence_barrier_init();
@@ -187,6 +187,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_kb);
     prefetch_tmap(&tm_vb);
     prefetch_tmap(&tm_dq);
+    prefetch_tmap(&tm_dk);
+    prefetch_tmap(&tm_dv);
   }
   tc_fence_before();
   __syncthreads();
@@ -428,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t s_cols = lane_base + C::kColS + 64 * half;
     const uint32_t dp_cols = lane_base + C::kColDP + 64 * half;
     const uint32_t ds_panel = smem_u32(smem + C::kDS) + half * 16384;
-    uint32_t qc = 0, gstep = 0, items = 0;
+    uint32_t qc = 0, gstep = 0, items = 0, stg = 0;
     bool ok = true;
     for (uint32_t k = 0; ok; ++k) {
       int w = 0;
@@ -520,30 +522,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       qc += nsteps;
-      // dV (columns-0 group) or dK (columns-64 group) of this key tile -> global rows.
+      // dV (columns-0 group) or dK (columns-64 group) of this key tile ->
+      // global rows: 32-column chunks staged in this group's half of the dS
+      // buffer (free once the unit's MMAs are done; the 128-byte swizzled
+      // layout of a [128 rows][32 fp32] TMA box) and reduce-added by one
+      // thread with TMA. Rows of keys past the tile hold zeros.
       ok = mbar_wait(&bar_dkdv_full, items & 1, wc);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-      const size_t gbase = ((size_t)key * p.hkv + it.g) * D;
-      float* dst = (half == 0 ? p.dv : p.dk) + gbase;
       const uint32_t src_col = lane_base + (half == 0 ? C::kColDV : C::kColDK);
       const float mul = half == 0 ? 1.f : p.scale;
+      const CUtensorMap* tm_out = half == 0 ? &tm_dv : &tm_dk;
 #pragma unroll 1
-      for (int cc = 0; cc < D / 32; ++cc) {
+      for (int cc = 0; cc < D / 32 && ok; ++cc, ++stg) {
         float v[32];
         tmem_ld32(src_col + cc * 32, v);
         tmem_ld_wait();
-        if (key_valid) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            red_add_v4(dst + cc * 32 + 4 * e, v[4 * e] * mul, v[4 * e + 1] * mul, v[4 * e + 2] * mul,
-                       v[4 * e + 3] * mul);
+        if (stg > 0) {  // the previous chunk's reduce has read the staging tile
+          ok = mbar_wait(&bar_stg_free[half], (stg - 1) & 1, wc);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         }
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const float a0 = key_valid ? v[4 * q4] * mul : 0.f, a1 = key_valid ? v[4 * q4 + 1] * mul : 0.f;
+          const float a2 = key_valid ? v[4 * q4 + 2] * mul : 0.f, a3 = key_valid ? v[4 * q4 + 3] * mul : 0.f;
+          st_shared_v4(ds_panel + sw128_offset(kr, q4), __float_as_uint(a0), __float_as_uint(a1),
+                       __float_as_uint(a2), __float_as_uint(a3));
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bar_stg_full[half]);
+        if (kr == 0) {
+          ok = mbar_wait(&bar_stg_full[half], stg & 1, wc);
+          if (ok) {
+            tma_reduce_add_3d(tm_out, smem + C::kDS + half * 16384, cc * 32, it.g, it.key0);
+            bulk_commit();
+            bulk_wait_read_all();
+          }
+          mbar_arrive(&bar_stg_free[half]);
+        }
+        ok = __all_sync(0xffffffffu, ok);  // the issuing lane's outcome, warp-wide
       }
+      // The last chunk's tile is read before dS of the next unit lands there.
+      if (ok) ok = mbar_wait(&bar_stg_free[half], (stg - 1) & 1, wc);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_before();
       mbar_arrive(&bar_dkdv_free);
       ++items;
     }
+    if (kr == 0) bulk_wait_all();  // this thread's reduces are complete before the CTA exits
   } else {
     // ------------------------------------------------------------ dQ drain
     // Thread r holds query row q0 + r. Each 32-column chunk goes to one of two
@@ -643,7 +669,7 @@ static int launch_bwd_impl(const BwdLaunch& a, cudaStream_t st) {
   if (n_work == 0) return FCP_OK;
   const int grid = n_work < a.num_sms ? n_work : a.num_sms;
   attn_bwd_kernel<D><<<grid, kThreads, C::kSmem, st>>>(a.tm_q, a.tm_do, a.tm_k, a.tm_v, a.tm_kb,
-                                                      a.tm_vb, a.tm_dq, a.p);
+                                                      a.tm_vb, a.tm_dq, a.tm_dk, a.tm_dv, a.p);
   return cudaGetLastError() == cudaSuccess ? FCP_OK : FCP_ERR_CUDA;
 }
 

@@ -56,6 +56,7 @@ struct BwdParams {
 struct BwdLaunch {
   CUtensorMap tm_q, tm_do, tm_k, tm_v, tm_kb, tm_vb;
   CUtensorMap tm_dq;  // dQ fp32 [T][Hq][d], boxes of 32 x 1 x 128 (reduce-add target)
+  CUtensorMap tm_dk, tm_dv;  // dK, dV fp32 [T][Hkv][d], same boxes (reduce-add targets)
   BwdParams p;
   int d;
   int num_sms;
