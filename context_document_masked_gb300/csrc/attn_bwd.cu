@@ -269,8 +269,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int u = 0; u < 4; ++u) {
           const int r = lane + 32 * u;
           const bool valid = r < q_rows;
-          st[r] = valid ? __ldg(p.lse + (size_t)h * p.T + q0 + r) * kLog2e : INFINITY;
-          st[128 + r] = valid ? __ldg(p.delta + (size_t)h * p.T + q0 + r) : 0.f;
+          // Stored negated (-LSE log2 e, -D): the compute warps add them with
+          // packed f32x2 arithmetic. Rows past the piece get P = 0.
+          st[r] = valid ? -__ldg(p.lse + (size_t)h * p.T + q0 + r) * kLog2e : -INFINITY;
+          st[128 + r] = valid ? -__ldg(p.delta + (size_t)h * p.T + q0 + r) : 0.f;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_q_full[s]);
@@ -455,27 +457,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const float4* st4 = reinterpret_cast<const float4*>(stat + s * 256 + 64 * half);
         uint32_t pk[32];
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          float v[32];
-          tmem_ld32(s_cols + cc * 32, v);
+        {
+          // Both 32-column halves of this group's S^T in flight together.
+          float va[32], vb[32];
+          tmem_ld32(s_cols, va);
+          tmem_ld32(s_cols + 32, vb);
           tmem_ld_wait();
+          const uint64_t c2 = f2(p.scale_log2, p.scale_log2);
 #pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            const int col = cc * 32 + e;
-            const float4 l4 = st4[col >> 2];
-            float p0 = ex2(fmaf(v[e], p.scale_log2, -l4.x));
-            float p1 = ex2(fmaf(v[e + 1], p.scale_log2, -l4.y));
-            float p2 = ex2(fmaf(v[e + 2], p.scale_log2, -l4.z));
-            float p3 = ex2(fmaf(v[e + 3], p.scale_log2, -l4.w));
+          for (int e = 0; e < 64; e += 4) {
+            const float* v = e < 32 ? va + e : vb + (e - 32);
+            const float4 l4 = st4[e >> 2];  // -LSE log2 e of the four query columns
+            float p0, p1, p2, p3;
+            f2_split(f2_fma(f2(v[0], v[1]), c2, f2(l4.x, l4.y)), p0, p1);
+            f2_split(f2_fma(f2(v[2], v[3]), c2, f2(l4.z, l4.w)), p2, p3);
+            p0 = ex2(p0);
+            p1 = ex2(p1);
+            p2 = ex2(p2);
+            p3 = ex2(p3);
             if (!unmasked) {
-              if (!key_valid || col < lim) p0 = 0.f;
-              if (!key_valid || col + 1 < lim) p1 = 0.f;
-              if (!key_valid || col + 2 < lim) p2 = 0.f;
-              if (!key_valid || col + 3 < lim) p3 = 0.f;
+              if (!key_valid || e < lim) p0 = 0.f;
+              if (!key_valid || e + 1 < lim) p1 = 0.f;
+              if (!key_valid || e + 2 < lim) p2 = 0.f;
+              if (!key_valid || e + 3 < lim) p3 = 0.f;
             }
-            pk[col >> 1] = pack_f16(p0, p1);
-            pk[(col >> 1) + 1] = pack_f16(p2, p3);
+            pk[e >> 1] = pack_f16(p0, p1);
+            pk[(e >> 1) + 1] = pack_f16(p2, p3);
           }
         }
         {
@@ -502,9 +509,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; e += 4) {
             const int col = cc * 32 + e;
-            const float4 d4 = st4[32 + (col >> 2)];
-            const __half2 x01 = __floats2half2_rn(v[e] - d4.x, v[e + 1] - d4.y);
-            const __half2 x23 = __floats2half2_rn(v[e + 2] - d4.z, v[e + 3] - d4.w);
+            const float4 d4 = st4[32 + (col >> 2)];  // -D of the four query columns
+            float a0, a1, a2, a3;
+            f2_split(f2_add(f2(v[e], v[e + 1]), f2(d4.x, d4.y)), a0, a1);
+            f2_split(f2_add(f2(v[e + 2], v[e + 3]), f2(d4.z, d4.w)), a2, a3);
+            const __half2 x01 = __floats2half2_rn(a0, a1);
+            const __half2 x23 = __floats2half2_rn(a2, a3);
             const uint32_t p01 = pk[col >> 1], p23 = pk[(col >> 1) + 1];
             const __half2 r01 = __hmul2(*reinterpret_cast<const __half2*>(&p01), x01);
             const __half2 r23 = __hmul2(*reinterpret_cast<const __half2*>(&p23), x23);
