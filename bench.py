@@ -42,8 +42,8 @@ BWD_TRAFFIC = {
     "sources": ["context_document_masked_gb300/csrc/attn_bwd.cu", "context_document_masked_gb300/csrc/copy_kernels.cu",
                 "context_document_masked_gb300/csrc/sm103.cuh", "context_document_masked_gb300/csrc/kernels.h",
                 "context_document_masked_gb300/csrc/api.cu"],
-    "sha256": "f43f06851e21ef4192066b0687b75bce19ec1ed8d81c3951b6880f28e6900d18",
-    "bytes": (2.741944 + 1.447788 + 1.087363 + 1.043690) * 1e9,
+    "sha256": "041b7fd88a01fd3430890917f4bb8d386940a63cd416e5115860f929908b6375",
+    "bytes": (2.776394 + 1.469725 + 1.087365 + 1.044097) * 1e9,
 }
 
 
