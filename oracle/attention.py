@@ -113,11 +113,12 @@ def attention_bruteforce(q, k, v, cu, scale=None, key_allowed=None):
     return o, lse
 
 
-def _doc_rows_fwd(qd, kd, vd, scale, key_lo, key_hi, row_chunk):
+def _doc_rows_fwd(qd, kd, vd, scale, key_lo, key_hi, row_chunk, key_ok=None):
     """Forward for one document and one head pair.
 
     qd [L,d], kd/vd [L,d] (document-local). Keys restricted to the local index
-    window [key_lo, key_hi). Returns o [L,d], lse [L].
+    window [key_lo, key_hi) and, if given, to the local keys with key_ok True.
+    Returns o [L,d], lse [L].
     """
     L = qd.shape[0]
     o = np.zeros_like(qd)
@@ -127,6 +128,8 @@ def _doc_rows_fwd(qd, kd, vd, scale, key_lo, key_hi, row_chunk):
         r1 = min(L, r0 + row_chunk)
         ii = np.arange(r0, r1)
         allowed = (jj[None, :] <= ii[:, None]) & (jj[None, :] >= key_lo) & (jj[None, :] < key_hi)
+        if key_ok is not None:
+            allowed &= key_ok[None, :]
         s = scale * (qd[r0:r1] @ kd.T)
         p, lse[r0:r1] = _softmax_rows(s, allowed)
         o[r0:r1] = p @ vd
@@ -134,13 +137,16 @@ def _doc_rows_fwd(qd, kd, vd, scale, key_lo, key_hi, row_chunk):
 
 
 def attention_per_doc(q, k, v, cu, scale=None, docs=None, heads=None,
-                      key_range=None, row_chunk=2048):
+                      key_range=None, row_chunk=2048, key_allowed=None):
     """Per-document dense causal attention (the same definition, one document
     at a time).
 
     docs: iterable of document indices to compute (default all); heads: query
     heads to compute (default all); key_range: (a, b) global key window for a
-    partial KV block. Rows/heads not computed are left as NaN so that a caller
+    partial KV block; key_allowed: optional bool [T] restricting the key set
+    further (e.g. to the keys one CP owner holds: the block a ring step
+    delivers, "LLM Context Parallel in Production", "Ring Attention").
+    Rows/heads not computed are left as NaN so that a caller
     cannot mistake them for results.
     Returns O [T,Hq,d], LSE [Hq,T] float64.
     """
@@ -163,9 +169,10 @@ def attention_per_doc(q, k, v, cu, scale=None, docs=None, heads=None,
         if key_range is not None:
             lo = min(max(key_range[0] - s0, 0), s1 - s0)
             hi = min(max(key_range[1] - s0, 0), s1 - s0)
+        ok = None if key_allowed is None else np.asarray(key_allowed, dtype=bool)[s0:s1]
         for h in heads:
             g = h // G
-            oo, ll = _doc_rows_fwd(q[s0:s1, h], k[s0:s1, g], v[s0:s1, g], scale, lo, hi, row_chunk)
+            oo, ll = _doc_rows_fwd(q[s0:s1, h], k[s0:s1, g], v[s0:s1, g], scale, lo, hi, row_chunk, ok)
             o[s0:s1, h] = oo
             lse[h, s0:s1] = ll
     return o, lse

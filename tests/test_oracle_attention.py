@@ -124,6 +124,55 @@ def test_merge_over_arbitrary_key_partition():
     np.testing.assert_allclose(lm, lse, atol=1e-12, rtol=0)
 
 
+@pytest.mark.parametrize("lengths", MIXES)
+def test_per_doc_key_mask_equals_bruteforce(lengths):
+    """The per-document form with a key mask (the keys one CP owner holds)
+    against the full T x T mask of the brute-force form; rows left without a
+    key get O = 0, LSE = -inf in both."""
+    cu, q, k, v = _inputs(lengths)
+    T = int(cu[-1])
+    mask = np.random.default_rng(T).random(T) < 0.4
+    ob, lb = A.attention_bruteforce(q, k, v, cu, key_allowed=mask)
+    op, lp = A.attention_per_doc(q, k, v, cu, key_allowed=mask)
+    np.testing.assert_allclose(op, ob, atol=1e-12, rtol=0)
+    assert np.array_equal(np.isneginf(lp), np.isneginf(lb))
+    fin = np.isfinite(lb)
+    np.testing.assert_allclose(lp[fin], lb[fin], atol=1e-12, rtol=0)
+
+
+@pytest.mark.parametrize("policy", ["llama3", "perdoc", "hybrid"])
+def test_merge_over_ring_owner_blocks(policy):
+    """Ring order ("LLM Context Parallel in Production", "Ring Attention"): at
+    step s shard j holds shard (j - s) mod N's KV block. For every shard's
+    rows, merging the N step partials (each over one owner's keys) gives the
+    unsplit result."""
+    from oracle import plan as P
+    lengths = [40, 7, 1, 60, 19, 33]
+    cu, q, k, v = _inputs(lengths)
+    N = 4
+    T = int(cu[-1])
+    pad = (-T) % (2 * N)
+    if pad:  # the Llama3 split needs T % 2N == 0
+        lengths = lengths[:-1] + [lengths[-1] + pad]
+        cu, q, k, v = _inputs(lengths)
+        T = int(cu[-1])
+    plan = P.make_plan(lengths, N, policy)
+    owner = np.full(T, -1)
+    for j, sh in enumerate(plan.shards):
+        for pc in sh.pieces:
+            owner[pc.start:pc.end] = j
+    assert (owner >= 0).all()
+    o_full, l_full = A.attention_per_doc(q, k, v, cu)
+    for j in range(N):
+        rows = np.array(plan.query_indices(j), dtype=np.int64)
+        parts = [A.attention_per_doc(q, k, v, cu, key_allowed=owner == (j - s) % N) for s in range(N)]
+        o_parts = np.stack([p_[0][rows] for p_ in parts])
+        l_parts = np.stack([p_[1][:, rows] for p_ in parts])
+        om, lm = A.merge(o_parts, l_parts)
+        np.testing.assert_allclose(om, o_full[rows], atol=1e-12, rtol=0)
+        np.testing.assert_allclose(lm, l_full[:, rows], atol=1e-12, rtol=0)
+
+
 def test_merge_all_empty_rows():
     o_parts = np.zeros((3, 2, 1, 4))
     lse_parts = np.full((3, 1, 2), -np.inf)
