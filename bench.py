@@ -244,6 +244,7 @@ def run_gpu(args):
     legs = set(args.legs.split(","))
     # Merge over the CP owners' key blocks (ring-style partials), same workload.
     merge = _bench_merge(s, q, k, v, w, torch, fcp, pk) if "merge" in legs else None
+    ring = _bench_ring(s, q, k, v, w, pairs, torch, fcp) if "ring" in legs else None
 
     # End to end through the public API: pinned host inputs -> device, plan,
     # gather, forward, backward, results back to pinned host buffers.
@@ -283,6 +284,7 @@ def run_gpu(args):
                    "frac_hbm": round(gather_bytes / (per["gather"] * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
                    "bytes": gather_bytes, "remote_rows": remote_rows},
         "merge": merge,
+        "ring": ring,
         "useful_pairs": pairs,
         "imbalance": policies,
         "clocks": clk.summary(),
@@ -293,6 +295,54 @@ def run_gpu(args):
     print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
+
+
+def _bench_ring(s, q, k, v, w, pairs, torch, fcp):
+    """The forward three ways, same workload, fp32 output ("LLM Context
+    Parallel in Production", "Ring Attention"; FlashCP §2.2 and §4 on the cost
+    of blockwise ring execution): (a) gather of the received keys + one
+    forward over them (the path of the timed step), (b) the fused ring (every
+    owner's keys read in ring order in one pass, no gather), (c) one partial
+    forward per ring step + fcp_merge of the N partials."""
+    T, hq, d, N = w.T, w.Hq, w.d, w.cp
+    dev = q.device
+    out = torch.empty(T, hq, d, dtype=torch.float32, device=dev)
+    lse = torch.empty(hq, T, dtype=torch.float32, device=dev)
+    o_parts = torch.empty(N, T, hq, d, dtype=torch.float32, device=dev)
+    l_parts = torch.empty(N, hq, T, dtype=torch.float32, device=dev)
+    mo = torch.empty(T, hq, d, dtype=torch.bfloat16, device=dev)
+    ml = torch.empty(hq, T, dtype=torch.float32, device=dev)
+
+    def gathered():
+        s.gather(k, v)
+        s.forward(q, k, v, out=out, lse=lse)
+
+    def fused():
+        s.forward_ring(q, k, v, ring_step=-1, out=out, lse=lse)
+
+    def stepwise():
+        for st in range(N):
+            s.forward_ring(q, k, v, ring_step=st, out=o_parts[st], lse=l_parts[st])
+        fcp.merge(o_parts, l_parts, mo, ml)
+
+    res = {}
+    for name, fn in (("gather_then_forward", gathered), ("ring_fused", fused), ("ring_steps_then_merge", stepwise)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n = 10
+        e0.record()
+        for _ in range(n):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / n
+        res[name] = {"ms": round(ms, 4), "tflops": round(4.0 * d * hq * pairs / (ms * 1e-3) / 1e12, 2)}
+    if s.device_status() != 0:
+        raise RuntimeError("device status reports a failed wait in the ring leg")
+    res["note"] = "useful fwd FLOPs / time; (c) includes the N partial forwards and the merge"
+    return res
 
 
 def _bench_merge(s, q, k, v, w, torch, fcp, pk):
@@ -434,8 +484,8 @@ def main():
     ap.add_argument("--impl", default="fcp", choices=["fcp", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=3.0)
-    ap.add_argument("--legs", default="step,merge,e2e,cpu",
-                    help="parts to run: step (always), merge, e2e, cpu; e.g. 'step' for profiling")
+    ap.add_argument("--legs", default="step,merge,ring,e2e,cpu",
+                    help="parts to run: step (always), merge, ring, e2e, cpu; e.g. 'step' for profiling")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "fcp":
         args.warmup = 3

@@ -264,10 +264,15 @@ int fcp_gather_kv(const void* k, const void* v, const fcp_dev_plan* plan, int32_
                             static_cast<cudaStream_t>(stream));
 }
 
-int fcp_attn_fwd(const void* q, const void* k, const void* v, const void* kbuf, const void* vbuf,
-                 const fcp_dev_plan* plan, int32_t shard, int32_t kv_lo, int32_t kv_hi,
-                 fcp_dims dims, int32_t out_dtype, void* out, float* lse, void* ws,
-                 int64_t ws_bytes, void* stream) {
+// Forward over the plan's gathered key layout (ring < -1: own rows from K/V,
+// received rows from kbuf/vbuf) or in ring order (ring >= -1: every needed key
+// from its owner's rows of K/V, owners visited by ring distance; ring = -1 all
+// of them in one pass, ring = s only the keys of owner (shard - s) mod N).
+static int attn_fwd_impl(const void* q, const void* k, const void* v, const void* kbuf, const void* vbuf,
+                         const fcp_dev_plan* plan, int32_t shard, int32_t kv_lo, int32_t kv_hi,
+                         fcp_dims dims, int32_t out_dtype, void* out, float* lse, void* ws,
+                         int64_t ws_bytes, void* stream, int32_t ring) {
+  const bool ring_order = ring >= -1;
   int st = check_dev_plan(plan, shard);
   if (st) return st;
   const Plan* p = plan->host;
@@ -277,7 +282,8 @@ int fcp_attn_fwd(const void* q, const void* k, const void* v, const void* kbuf, 
   if (kv_lo < 0 || kv_hi > dims.T || kv_lo > kv_hi) return FCP_ERR_INVALID_ARG;
   const WsLayout wl = ws_layout(dims, p->total_remote);
   if (ws_bytes < wl.total) return FCP_ERR_CAPACITY;
-  const int64_t rrows = remote_rows_of(p, shard);
+  if (ring_order && ring >= plan->n_shards) return FCP_ERR_INVALID_ARG;
+  const int64_t rrows = ring_order ? 0 : remote_rows_of(p, shard);
   if (rrows > 0 && (!kbuf || !vbuf)) return FCP_ERR_INVALID_ARG;
   for (const void* ptr : {q, k, v, (const void*)out, (const void*)lse, (const void*)ws})
     if (!aligned16(ptr)) return FCP_ERR_INVALID_ARG;
@@ -307,8 +313,9 @@ int fcp_attn_fwd(const void* q, const void* k, const void* v, const void* kbuf, 
     ok = ok && make_map(&a.tm_kb, k, dims.d, dims.hkv, dims.T) && make_map(&a.tm_vb, v16, dims.d, dims.hkv, dims.T, true);
   if (!ok) return FCP_ERR_CUDA;
   fcp::FwdParams& fp = a.p;
-  fp.pieces = table(plan, fcp::TB_PIECES);
-  fp.segs = table(plan, fcp::TB_SEGS);
+  fp.pieces = table(plan, ring_order ? fcp::TB_RPIECES : fcp::TB_PIECES);
+  fp.segs = table(plan, ring_order ? fcp::TB_RSEGS : fcp::TB_SEGS);
+  fp.seg_filter = ring_order ? ring : -1;
   fp.tiles = table(plan, fcp::TB_FTILES);
   if (shard < 0) {
     fp.order = table(plan, fcp::TB_FORDER);
@@ -318,7 +325,7 @@ int fcp_attn_fwd(const void* q, const void* k, const void* v, const void* kbuf, 
     const int32_t t0 = host_at(p, fcp::TB_FSHARD, shard), t1 = host_at(p, fcp::TB_FSHARD, shard + 1);
     fp.order = table(plan, fcp::TB_IDENT) + t0;
     fp.n_items = t1 - t0;
-    fp.kbuf_shift = (int32_t)p->shards[shard].kbuf_base;
+    fp.kbuf_shift = ring_order ? 0 : (int32_t)p->shards[shard].kbuf_base;
   }
   fp.kv_lo = kv_lo;
   fp.kv_hi = kv_hi;
@@ -335,6 +342,22 @@ int fcp_attn_fwd(const void* q, const void* k, const void* v, const void* kbuf, 
   a.d = dims.d;
   a.num_sms = num_sms();
   return fcp::launch_attn_fwd(a, cs);
+}
+
+int fcp_attn_fwd(const void* q, const void* k, const void* v, const void* kbuf, const void* vbuf,
+                 const fcp_dev_plan* plan, int32_t shard, int32_t kv_lo, int32_t kv_hi,
+                 fcp_dims dims, int32_t out_dtype, void* out, float* lse, void* ws,
+                 int64_t ws_bytes, void* stream) {
+  return attn_fwd_impl(q, k, v, kbuf, vbuf, plan, shard, kv_lo, kv_hi, dims, out_dtype, out, lse, ws,
+                       ws_bytes, stream, -2);
+}
+
+int fcp_attn_fwd_ring(const void* q, const void* k, const void* v, const fcp_dev_plan* plan,
+                      int32_t shard, int32_t ring_step, fcp_dims dims, int32_t out_dtype, void* out,
+                      float* lse, void* ws, int64_t ws_bytes, void* stream) {
+  if (ring_step < -1) return FCP_ERR_INVALID_ARG;
+  return attn_fwd_impl(q, k, v, nullptr, nullptr, plan, shard, 0, dims.T, dims, out_dtype, out, lse, ws,
+                       ws_bytes, stream, ring_step);
 }
 
 int fcp_merge(const float* o_parts, const float* lse_parts, int32_t B, int64_t rows, int32_t hq,

@@ -64,15 +64,17 @@ struct FwdCfg {
   static constexpr uint32_t kColO = 256;                 // O_i at 256 + i*D
 };
 
-// Key tiles of one query tile: every segment of the piece, clipped to the key
-// block [lo, hi) and to keys <= q_last, cut into tiles of 128 keys.
+// Key tiles of one query tile: every segment of the piece (those whose first
+// field equals `filter`, if filter >= 0), clipped to the key block [lo, hi)
+// and to keys <= q_last, cut into tiles of 128 keys. Segments may come in any
+// key order (the ring order lists them by owner).
 struct Walker {
   const int32_t* seg;
-  int s, s_end, q_last, lo, hi, shift;
+  int s, s_end, q_last, lo, hi, shift, filter;
   int pos, end, ks, src, srow;
 
   __device__ void init(const int32_t* segs, int seg_begin, int seg_count, int q_last_, int lo_,
-                       int hi_, int shift_) {
+                       int hi_, int shift_, int filter_) {
     seg = segs;
     s = seg_begin - 1;
     s_end = seg_begin + seg_count;
@@ -80,6 +82,7 @@ struct Walker {
     lo = lo_;
     hi = hi_;
     shift = shift_;
+    filter = filter_;
     pos = end = 0;
   }
   __device__ bool next(int& src_o, int& row_o, int& key_o, int& n_o) {
@@ -87,12 +90,9 @@ struct Walker {
       if (++s >= s_end) return false;
       const int* g = seg + 4 * s;
       ks = __ldg(g + 2);
-      if (ks > q_last) {
-        s = s_end;
-        return false;
-      }
-      const int len = __ldg(g + 3);
       src = __ldg(g + 0);
+      if (ks > q_last || (filter >= 0 && src != filter)) continue;  // pos >= end still holds
+      const int len = __ldg(g + 3);
       srow = __ldg(g + 1) - (src ? shift : 0);
       pos = max(ks, lo);
       end = min(min(ks + len, hi), q_last + 1);
@@ -107,12 +107,12 @@ struct Walker {
 };
 
 __device__ __forceinline__ int count_key_tiles(const int32_t* segs, int seg_begin, int seg_count,
-                                               int q_last, int lo, int hi) {
+                                               int q_last, int lo, int hi, int filter) {
   int n = 0;
   for (int s = seg_begin; s < seg_begin + seg_count; ++s) {
     const int* g = segs + 4 * s;
     const int ks = __ldg(g + 2);
-    if (ks > q_last) break;
+    if (ks > q_last || (filter >= 0 && __ldg(g) != filter)) continue;
     const int a = max(ks, lo);
     const int e = min(min(ks + __ldg(g + 3), hi), q_last + 1);
     if (e > a) n += (e - a + 127) / 128;
@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = ring.put<true>(k++, w, wc)) || w >= n_work) break;
         const WorkItem it = decode(p, w);
         const int q_last = it.q_start + it.q_rows - 1;
-        const int nt = count_key_tiles(p.segs, it.seg_begin, it.seg_count, q_last, p.kv_lo, p.kv_hi);
+        const int nt = count_key_tiles(p.segs, it.seg_begin, it.seg_count, q_last, p.kv_lo, p.kv_hi, p.seg_filter);
         if (nt == 0) continue;
         if (q_iter > 0 && !(ok = mbar_wait_inline(&bar_q_empty, (q_iter - 1) & 1, wc))) break;
         mbar_arrive_expect_tx(&bar_q_full, 2 * C::kTileBytes);
@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         it.q_start);
         ++q_iter;
         Walker wk;
-        wk.init(p.segs, it.seg_begin, it.seg_count, q_last, p.kv_lo, p.kv_hi, p.kbuf_shift);
+        wk.init(p.segs, it.seg_begin, it.seg_count, q_last, p.kv_lo, p.kv_hi, p.kbuf_shift, p.seg_filter);
         int src, row, key, n;
         while (ok && wk.next(src, row, key, n)) {
           for (int kv = 0; kv < 2; ++kv) {
@@ -278,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (w >= n_work) break;
         const WorkItem it = decode(p, w);
         const int q_last = it.q_start + it.q_rows - 1;
-        const int nt = count_key_tiles(p.segs, it.seg_begin, it.seg_count, q_last, p.kv_lo, p.kv_hi);
+        const int nt = count_key_tiles(p.segs, it.seg_begin, it.seg_count, q_last, p.kv_lo, p.kv_hi, p.seg_filter);
         if (nt == 0) continue;
         if (!(ok = mbar_wait_inline(&bar_q_full, q_iter & 1, wc))) break;
         tc_fence_after();
@@ -348,14 +348,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (w >= n_work) break;
       const WorkItem it = decode(p, w);
       const int q_last = it.q_start + it.q_rows - 1;
-      const int nt = count_key_tiles(p.segs, it.seg_begin, it.seg_count, q_last, p.kv_lo, p.kv_hi);
+      const int nt = count_key_tiles(p.segs, it.seg_begin, it.seg_count, q_last, p.kv_lo, p.kv_hi, p.seg_filter);
       const int q = it.q_start + r;
       const bool row_valid = r < it.q_rows;
       const int head = it.h0 + i;
       float m_run = -INFINITY, l = 0.f;
       if (nt > 0) {
         Walker wk;
-        wk.init(p.segs, it.seg_begin, it.seg_count, q_last, p.kv_lo, p.kv_hi, p.kbuf_shift);
+        wk.init(p.segs, it.seg_begin, it.seg_count, q_last, p.kv_lo, p.kv_hi, p.kbuf_shift, p.seg_filter);
         int src, row, key, n;
         for (int t = 0; t < nt; ++t) {
           wk.next(src, row, key, n);

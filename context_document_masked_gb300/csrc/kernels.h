@@ -17,6 +17,7 @@ struct FwdParams {
   int32_t n_items;
   int32_t kbuf_shift;      // subtracted from received-key rows (one-shard launches)
   int32_t kv_lo, kv_hi;    // key block
+  int32_t seg_filter;      // -1: every key segment; else only segments whose first field equals it
   int32_t T, hq, hkv;
   float scale_log2;        // softmax scale * log2(e)
   int32_t out_f32;

@@ -164,6 +164,7 @@ extern "C" int fcp_attn_fwd_noalloc(const void* q, const void* k, const void* v,
   }
   fp.kv_lo = kv_lo;
   fp.kv_hi = kv_hi;
+  fp.seg_filter = -1;
   fp.T = dims.T;
   fp.hq = dims.hq;
   fp.hkv = dims.hkv;

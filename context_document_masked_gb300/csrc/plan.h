@@ -40,6 +40,8 @@ enum Table {
   TB_RSHARD,
   TB_IDENT,        // 0, 1, 2, ... (indirection for one-shard launches)
   TB_KBASE,        // N+1 kbuf row offsets
+  TB_RPIECES,      // TB_PIECES with seg_begin / seg_count into TB_RSEGS
+  TB_RSEGS,        // 4 ints: ring distance, src_row (= key_start), key_start, len
   TB_COUNT
 };
 

@@ -14,6 +14,7 @@
 // CTAs running at the same time then share one piece's query rows and keys
 // in L2, and the long rows start early.
 #include <algorithm>
+#include <array>
 #include <numeric>
 
 #include "plan.h"
@@ -191,6 +192,36 @@ void Plan::build_work_tables() {
   for (int32_t j = 0; j < N; ++j) kbase[j] = (int32_t)shards[j].kbuf_base;
   kbase[N] = (int32_t)total_remote;
 
+  // Ring order ("LLM Context Parallel in Production", "Ring Attention": at
+  // step s shard j holds the KV block of shard (j - s) mod N). A piece's
+  // needed keys [doc start, piece end) are cut into runs by the shard that
+  // owns them and listed by ring distance (j - owner) mod N, own keys first,
+  // each run read from K/V at its global rows.
+  std::vector<std::vector<std::array<int32_t, 3>>> doc_runs(D.size());  // (start, end, owner)
+  for (int32_t j = 0; j < N; ++j)
+    for (const Piece& p : shards[j].pieces) doc_runs[p.doc].push_back({p.start, p.end, j});
+  for (auto& v : doc_runs) std::sort(v.begin(), v.end());
+  std::vector<int32_t> rpieces, rsegs;
+  for (int32_t j = 0; j < N; ++j) {
+    for (const Piece& p : shards[j].pieces) {
+      std::vector<std::array<int32_t, 3>> runs;  // (distance, start, len)
+      for (const auto& r : doc_runs[p.doc]) {
+        if (r[0] >= p.end) break;
+        const int32_t e = std::min(r[1], p.end);
+        const int32_t dist = ((j - r[2]) % N + N) % N;
+        if (!runs.empty() && runs.back()[0] == dist && runs.back()[1] + runs.back()[2] == r[0])
+          runs.back()[2] += e - r[0];
+        else
+          runs.push_back({dist, r[0], e - r[0]});
+      }
+      std::stable_sort(runs.begin(), runs.end(),
+                       [](const std::array<int32_t, 3>& a, const std::array<int32_t, 3>& b) { return a[0] < b[0]; });
+      const int32_t begin = (int32_t)(rsegs.size() / 4);
+      for (const auto& r : runs) rsegs.insert(rsegs.end(), {r[0], r[1], r[1], r[2]});
+      rpieces.insert(rpieces.end(), {j, p.doc, p.start, p.end, off[p.doc], begin, (int32_t)runs.size(), 0});
+    }
+  }
+
   for (const Seg& g : segs) segs_flat.insert(segs_flat.end(), {g.src, g.src_row, g.key_start, g.len});
   dev.clear();
   append(dev, tab_off, tab_cnt, TB_PIECES, pieces, (int32_t)(pieces.size() / 8));
@@ -207,6 +238,8 @@ void Plan::build_work_tables() {
   append(dev, tab_off, tab_cnt, TB_RSHARD, rshard, N + 1);
   append(dev, tab_off, tab_cnt, TB_IDENT, ident, (int32_t)ident.size());
   append(dev, tab_off, tab_cnt, TB_KBASE, kbase, N + 1);
+  append(dev, tab_off, tab_cnt, TB_RPIECES, rpieces, (int32_t)(rpieces.size() / 8));
+  append(dev, tab_off, tab_cnt, TB_RSEGS, rsegs, (int32_t)(rsegs.size() / 4));
   while ((dev.size() * 4) % 256) dev.push_back(0);
 }
 

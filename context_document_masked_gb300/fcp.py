@@ -22,7 +22,7 @@ EXPORTED = (
     "fcp_strerror", "fcp_plan", "fcp_plan_free", "fcp_plan_shard", "fcp_plan_query_indices",
     "fcp_plan_stats", "fcp_plan_per_doc_flags", "fcp_plan_device_bytes", "fcp_plan_upload",
     "fcp_workspace_bytes", "fcp_gather_kv", "fcp_attn_fwd", "fcp_merge", "fcp_attn_bwd",
-    "fcp_get_device_status", "fcp_debug_set_wait_limit", "fcp_attn_fwd_noalloc",
+    "fcp_get_device_status", "fcp_debug_set_wait_limit", "fcp_attn_fwd_noalloc", "fcp_attn_fwd_ring",
 )
 
 
@@ -87,6 +87,8 @@ def _load():
         "fcp_gather_kv": (C.c_int, [vp, vp, C.POINTER(DevPlan), i32, i32, i32, vp, vp, vp]),
         "fcp_attn_fwd": (C.c_int, [vp, vp, vp, vp, vp, C.POINTER(DevPlan), i32, i32, i32, Dims, i32,
                                    vp, vp, vp, i64, vp]),
+        "fcp_attn_fwd_ring": (C.c_int, [vp, vp, vp, C.POINTER(DevPlan), i32, i32, Dims, i32, vp, vp, vp, i64,
+                                        vp]),
         "fcp_merge": (C.c_int, [vp, vp, i32, i64, i32, i32, vp, vp, vp]),
         "fcp_attn_bwd": (C.c_int, [vp, vp, vp, vp, vp, vp, i32, vp, vp, C.POINTER(DevPlan), i32,
                                    Dims, vp, vp, vp, vp, i64, vp]),
@@ -238,6 +240,21 @@ def attn_fwd(q, k, v, kbuf, vbuf, dplan: DevicePlan, shard: int, out, lse, ws, k
                              shard, kv_lo, T if kv_hi is None else kv_hi, dm, out_dtype, _ptr(out),
                              _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
            "fcp_attn_fwd")
+
+
+def attn_fwd_ring(q, k, v, dplan: DevicePlan, shard: int, ring_step: int, out, lse, ws, scale: float = 0.0,
+                  stream=None):
+    """fcp_attn_fwd_ring: every needed key read from its owner's rows of K/V,
+    owners in ring order; ring_step -1 = all owners in one pass, s >= 0 = the
+    partial result of ring step s."""
+    import torch
+    T, hq, d = q.shape
+    dm = Dims(T, hq, k.shape[1], d, scale)
+    out_dtype = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
+    _check(_lib.fcp_attn_fwd_ring(_ptr(q), _ptr(k), _ptr(v), C.byref(dplan.c), shard, ring_step, dm, out_dtype,
+                                  _ptr(out), _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(),
+                                  _stream(stream)),
+           "fcp_attn_fwd_ring")
 
 
 def attn_fwd_noalloc(q, k, v, kbuf, vbuf, dplan: DevicePlan, shard: int, out, lse, kv_lo: int = 0,

@@ -46,6 +46,18 @@ class CPAttention:
                      kv_lo=lo, kv_hi=hi, scale=self.scale, stream=stream)
         return out, lse
 
+    def forward_ring(self, q, k, v, ring_step: int = -1, shard: int = -1, out=None, lse=None,
+                     out_dtype=torch.bfloat16, stream=None):
+        """Forward in ring order without the gathered buffer: ring_step -1 visits
+        every owner's keys in one pass, s >= 0 gives ring step s's partial."""
+        if out is None:
+            out = torch.empty(self.T, self.hq, self.d, dtype=out_dtype, device=self.device)
+        if lse is None:
+            lse = torch.empty(self.hq, self.T, dtype=torch.float32, device=self.device)
+        fcp.attn_fwd_ring(q, k, v, self.dplan, shard, ring_step, out, lse, self.ws, scale=self.scale,
+                          stream=stream)
+        return out, lse
+
     def backward(self, q, k, v, out, lse, dout, shard: int = -1, dq=None, dk=None, dv=None,
                  zero_kv_grads: bool = True, stream=None):
         if dq is None:

@@ -224,6 +224,31 @@ int fcp_attn_fwd(const void* q, const void* k, const void* v, const void* kbuf,
                  void* out, float* lse, void* ws, int64_t ws_bytes, void* stream);
 
 /*
+ * fcp_attn_fwd_ring -- the same forward in ring order, without a gathered
+ * key buffer ([CPGuide] "Ring Attention": at step s of the ring, shard j
+ * holds the KV block of shard (j - s) mod N and merges its partial result by
+ * the online softmax; [FlashCP] §2.2 ("Reduced Kernel Efficiency") and §4
+ * attribute a cost to this blockwise execution and its partial-result
+ * processing, against the gather-then-compute design of fcp_gather_kv +
+ * fcp_attn_fwd).
+ * Every key a query needs is read from its owner's rows of k/v (owner = the
+ * shard that holds that token in the plan), owners visited in ring order
+ * (own rows first).
+ *   ring_step -1: all owners in one pass, the softmax state carried across
+ *             them (the fused ring: no partial results are stored). Output
+ *             equals fcp_attn_fwd's up to the summation order.
+ *             s in [0, N): only the keys of owner (j - s) mod N for each
+ *             query of shard j -- the partial (O, LSE) of ring step s, to be
+ *             combined with fcp_merge; a row with no such key gets O = 0,
+ *             LSE = -inf.
+ *   Other arguments as fcp_attn_fwd (no kbuf/vbuf, no key block). The
+ *   workspace is the same (its received-row part is unused).
+ */
+int fcp_attn_fwd_ring(const void* q, const void* k, const void* v, const fcp_dev_plan* plan,
+                      int32_t shard, int32_t ring_step, fcp_dims dims, int32_t out_dtype, void* out,
+                      float* lse, void* ws, int64_t ws_bytes, void* stream);
+
+/*
  * fcp_merge -- combine B partial results over disjoint key blocks
  * ([CPGuide] "Core Principle: Split Q, Circulate KV" and "Ring Attention":
  * online softmax keeps each block's row maximum and exponential sum).

@@ -96,6 +96,11 @@ def test_device_calls_validate_before_launch(lib):
     assert lib.raw_call("fcp_merge", None, None, 32, 10, 4, 128, None, None, None) == lib.ERR_INVALID_ARG
     assert lib.raw_call("fcp_merge", None, None, 2, 1 << 28, 4, 128, None, None, None) == lib.ERR_UNSUPPORTED
     assert lib.raw_call("fcp_get_device_status", None, None) == lib.ERR_INVALID_ARG
+    dm2 = lib.dims(64, 4, 2, 128)
+    assert lib.raw_call("fcp_attn_fwd_ring", None, None, None, None, -1, -1, dm2, 0,
+                        None, None, None, 0, None) == lib.ERR_INVALID_ARG   # null plan
+    assert lib.raw_call("fcp_attn_fwd_ring", None, None, None, None, -1, -2, dm2, 0,
+                        None, None, None, 0, None) == lib.ERR_INVALID_ARG   # ring_step < -1
     assert lib.workspace_bytes(lib.dims(1000, 8, 2, 128)) >= 256 + 8 * 1000 * 4 + 2 * 1000 * 8 * 128 * 2
     assert lib.strerror(lib.ERR_TIMEOUT) == "bounded device wait expired"
     del ctypes
