@@ -143,6 +143,11 @@ int fcp_plan_shard(const fcp_plan_t* plan, int32_t shard, fcp_shard_view* out) {
   out->useful_pairs = s.W;
   out->remote_rows = s.remote_rows;
   out->kbuf_base = s.kbuf_base;
+  out->fwd_tiles = s.fwd_tiles;
+  out->fwd_qtiles = s.fwd_qtiles;
+  out->fwd_masked = s.fwd_masked;
+  out->bwd_tiles = s.bwd_tiles;
+  out->bwd_ktiles = s.bwd_ktiles;
   return FCP_OK;
 }
 

@@ -22,6 +22,10 @@ struct Shard {
   std::vector<fcp_range> kv_need;
   std::vector<fcp_range> kv_remote;
   int64_t tokens = 0, W = 0, remote_rows = 0, kbuf_base = 0;
+  // Tiles the kernels visit (per query head): forward query x key tiles,
+  // forward query tiles, forward tiles needing a per-element mask; backward
+  // key x query tiles and backward key tiles.
+  int64_t fwd_tiles = 0, fwd_qtiles = 0, fwd_masked = 0, bwd_tiles = 0, bwd_ktiles = 0;
 };
 
 // Device table ids (index into fcp_dev_plan::tables / counts).

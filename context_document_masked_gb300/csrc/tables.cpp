@@ -37,6 +37,23 @@ int64_t count_key_tiles(const std::vector<Seg>& segs, int32_t seg_begin, int32_t
   return n;
 }
 
+// Key tiles of query tile [q0, q_last] that need a per-element mask: those
+// reaching past q0 (the diagonal) or shorter than a full tile (a segment end).
+int64_t count_masked_tiles(const std::vector<Seg>& segs, int32_t seg_begin, int32_t seg_count,
+                           int32_t q0, int32_t q_last) {
+  int64_t n = 0;
+  for (int32_t s = seg_begin; s < seg_begin + seg_count; ++s) {
+    const Seg& g = segs[s];
+    if (g.key_start > q_last) break;
+    const int32_t end = std::min<int64_t>((int64_t)g.key_start + g.len, (int64_t)q_last + 1);
+    for (int32_t k = g.key_start; k < end; k += kTileN) {
+      const int32_t nk = std::min(kTileN, end - k);
+      if (k + kTileN - 1 > q0 || nk < kTileN) ++n;
+    }
+  }
+  return n;
+}
+
 void append(std::vector<int32_t>& dev, int32_t* off, int32_t* cnt, int tb,
             const std::vector<int32_t>& data, int32_t n_entries) {
   while (dev.size() % 4) dev.push_back(0);  // 16-byte alignment of every table
@@ -111,6 +128,9 @@ void Plan::build_work_tables() {
         ftiles.insert(ftiles.end(), {piece_id, q0, qr, (int32_t)std::min<int64_t>(c, 1 << 30)});
         fcost.push_back(c);
         fpiece.push_back(piece_id);
+        shards[j].fwd_tiles += c;
+        shards[j].fwd_qtiles += 1;
+        shards[j].fwd_masked += count_masked_tiles(segs, seg_begin, seg_count, q0, q0 + qr - 1);
       }
       // Backward key tiles: every tile of every segment; the queries that see
       // it are the piece's rows at or after the tile start.
@@ -125,6 +145,8 @@ void Plan::build_work_tables() {
           btiles.insert(btiles.end(), {piece_id, s, key, kr, g.src, g.src_row + k0, qt_first, n_qt});
           bcost.push_back(n_qt);
           bpiece.push_back(piece_id);
+          shards[j].bwd_tiles += n_qt;
+          shards[j].bwd_ktiles += 1;
         }
       }
       for (int32_t a = p.start; a < p.end; a += kRowChunk)

@@ -42,7 +42,8 @@ class ShardView(C.Structure):
         ("n_need", C.c_int32), ("kv_need", C.POINTER(Range)),
         ("n_remote", C.c_int32), ("kv_remote", C.POINTER(Range)),
         ("tokens", C.c_int64), ("useful_pairs", C.c_int64), ("remote_rows", C.c_int64),
-        ("kbuf_base", C.c_int64),
+        ("kbuf_base", C.c_int64), ("fwd_tiles", C.c_int64), ("fwd_qtiles", C.c_int64),
+        ("fwd_masked", C.c_int64), ("bwd_tiles", C.c_int64), ("bwd_ktiles", C.c_int64),
     ]
 
 
@@ -150,6 +151,8 @@ class Plan:
             "pieces": rng(v.pieces, v.n_pieces), "kv_need": rng(v.kv_need, v.n_need),
             "kv_remote": rng(v.kv_remote, v.n_remote), "tokens": v.tokens,
             "useful_pairs": v.useful_pairs, "remote_rows": v.remote_rows, "kbuf_base": v.kbuf_base,
+            "fwd_tiles": v.fwd_tiles, "fwd_qtiles": v.fwd_qtiles, "fwd_masked": v.fwd_masked,
+            "bwd_tiles": v.bwd_tiles, "bwd_ktiles": v.bwd_ktiles,
         }
 
     def query_indices(self, j: int) -> np.ndarray:

@@ -86,6 +86,13 @@ typedef struct {
   int64_t useful_pairs;        /* sum of W_i = (2 p_i + s_i + 1) s_i / 2           */
   int64_t remote_rows;         /* rows in kv_remote                                */
   int64_t kbuf_base;           /* first row of this shard in an all-shards kbuf    */
+  /* Tiles of 128 x 128 the kernels visit for this shard, per query head
+   * (useful pairs only enter tiles that hold at least one):              */
+  int64_t fwd_tiles;           /* forward query-tile x key-tile pairs              */
+  int64_t fwd_qtiles;          /* forward query tiles                              */
+  int64_t fwd_masked;          /* forward tiles needing a per-element mask         */
+  int64_t bwd_tiles;           /* backward key-tile x query-tile pairs             */
+  int64_t bwd_ktiles;          /* backward key tiles (per KV head)                 */
 } fcp_shard_view;
 
 typedef struct {

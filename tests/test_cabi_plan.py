@@ -66,6 +66,57 @@ def test_cpp_planner_matches_oracle(lib, name, D, N, pol, R):
         np.testing.assert_array_equal(got.query_indices(j), np.asarray(ref.query_indices(j), dtype=np.int32))
 
 
+def _tile_counts(shard, cu, tile=128):
+    """The tiles the kernels visit for one oracle shard, derived from its
+    pieces and received ranges: a piece's keys [doc start, piece end) form
+    maximal runs held by the shard or received; the forward walks them per
+    query tile up to its last query, the backward takes every key tile of
+    every run with the piece's query tiles from the first that sees it."""
+    fwd = qt = masked = bwd = kt = 0
+    for pc in shard.pieces:
+        ds = int(cu[pc.doc])
+        runs, t = [], ds
+        while t < pc.end:
+            own = [o for o in shard.pieces if o.doc == pc.doc and o.start <= t < o.end]
+            rem = [r for r in shard.kv_remote if r[0] == pc.doc and r[1] <= t < r[2]]
+            e = min(own[0].end if own else rem[0][2], pc.end)
+            runs.append((t, e - t))
+            t = e
+        for q0 in range(pc.start, pc.end, tile):
+            q_last = min(q0 + tile, pc.end) - 1
+            qt += 1
+            for ks, ln in runs:
+                if ks > q_last:
+                    break
+                end = min(ks + ln, q_last + 1)
+                for k in range(ks, end, tile):
+                    fwd += 1
+                    masked += int(k + tile - 1 > q0 or end - k < tile)
+        n_qt_all = -(-(pc.end - pc.start) // tile)
+        for ks, ln in runs:
+            for k0 in range(0, ln, tile):
+                key = ks + k0
+                bwd += n_qt_all - (max(key, pc.start) - pc.start) // tile
+                kt += 1
+    return fwd, qt, masked, bwd, kt
+
+
+@pytest.mark.parametrize("name,D,N,pol,R", CASES[:20] + CASES[-40:], ids=[c[0] for c in CASES[:20] + CASES[-40:]])
+def test_tile_counts_per_shard(lib, name, D, N, pol, R):
+    """H6 metrics: the tiles each shard's kernels visit, against the walk
+    re-derived from the oracle plan; every useful pair lies in a visited tile."""
+    ref = P.make_plan(D, N, pol, R)
+    got = lib.Plan(D, N, pol, R)
+    cu = synth.cu_from_lengths(D)
+    for j in range(N):
+        s = got.shard(j)
+        f, q, m, b, k = _tile_counts(ref.shards[j], cu)
+        assert (s["fwd_tiles"], s["fwd_qtiles"], s["fwd_masked"], s["bwd_tiles"], s["bwd_ktiles"]) == (f, q, m, b, k)
+        assert s["useful_pairs"] <= s["fwd_tiles"] * 128 * 128
+        assert s["useful_pairs"] <= s["bwd_tiles"] * 128 * 128
+        assert s["fwd_masked"] <= s["fwd_tiles"]
+
+
 def test_plan_errors(lib):
     with pytest.raises(lib.FcpError) as e:
         lib.Plan([5, 4], 2, "llama3")
