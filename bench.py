@@ -245,6 +245,7 @@ def run_gpu(args):
     # Merge over the CP owners' key blocks (ring-style partials), same workload.
     merge = _bench_merge(s, q, k, v, w, torch, fcp, pk) if "merge" in legs else None
     ring = _bench_ring(s, q, k, v, w, pairs, torch, fcp) if "ring" in legs else None
+    shards = _bench_shards(torch, dev) if "shards" in legs else None
 
     # End to end through the public API: pinned host inputs -> device, plan,
     # gather, forward, backward, results back to pinned host buffers.
@@ -255,7 +256,7 @@ def run_gpu(args):
             dist.destroy_process_group()
         return
     policies = {}
-    for pol in ("llama3", "perdoc", "wholedoc", "hybrid"):
+    for pol in ("llama3", "perdoc", "wholedoc", "hybrid", "hybrid_tiles"):
         try:
             st = fcp.Plan(D, w.cp, pol).stats()
             policies[pol] = {"imbalance": round(st["imbalance"], 4), "remote_rows": st["remote_rows_total"],
@@ -285,6 +286,7 @@ def run_gpu(args):
                    "bytes": gather_bytes, "remote_rows": remote_rows},
         "merge": merge,
         "ring": ring,
+        "shards": shards,
         "useful_pairs": pairs,
         "imbalance": policies,
         "clocks": clk.summary(),
@@ -295,6 +297,49 @@ def run_gpu(args):
     print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
+
+
+def _bench_shards(torch, dev):
+    """Per-shard kernel time against W and against the tiles visited, one shard
+    per launch (context_document_masked_gb300.calibrate): the 32K packed
+    workload under Per-Doc and the 64K short-document workload under the four
+    policies."""
+    from context_document_masked_gb300 import calibrate as cal
+    rows, per_policy = [], {}
+    for cfg, policies in ((2, ("perdoc",)), (4, ("llama3", "perdoc", "wholedoc", "hybrid", "hybrid_tiles")),
+                          (3, ("perdoc", "hybrid", "hybrid_tiles"))):
+        w = synth.WORKLOADS[cfg]
+        D = synth.doc_lengths(cfg)
+        q, k, v = synth.make_qkv(w.T, w.Hq, w.Hkv, w.d, seed=2000 + cfg, device=dev)
+        do = synth.make_dout(w.T, w.Hq, w.d, seed=2000 + cfg, device=dev)
+        for pol in policies:
+            r = cal.shard_times(D, w.cp, pol, q, k, v, do)
+            for x in r:
+                x["workload"], x["policy"] = w.name, pol
+            rows += r
+            per_policy[f"{w.name}/{pol}"] = {
+                "imbalance_pairs": round(cal.imbalance([x["pairs"] for x in r]), 4),
+                "imbalance_fwd_tiles": round(cal.imbalance([x["fwd_tiles"] for x in r]), 4),
+                "imbalance_time": round(cal.imbalance([x["fwd_ms"] + x["bwd_ms"] for x in r]), 4),
+                "max_shard_ms": round(max(x["fwd_ms"] + x["bwd_ms"] for x in r), 4)}
+        del q, k, v, do
+    fits = {
+        "fwd~pairs": cal.fit(rows, ("pairs",), "fwd_ms"),
+        "fwd~tiles+qtiles": cal.fit(rows, ("fwd_tiles", "fwd_qtiles"), "fwd_ms"),
+        "bwd~pairs": cal.fit(rows, ("pairs",), "bwd_ms"),
+        "bwd~tiles+ktiles": cal.fit(rows, ("bwd_tiles", "bwd_ktiles"), "bwd_ms"),
+    }
+    fits["fwd+bwd~tiles+qtiles"] = cal.fit([dict(r, both=r["fwd_ms"] + r["bwd_ms"]) for r in rows],
+                                           ("fwd_tiles", "fwd_qtiles"), "both")
+    for f in fits.values():
+        f["coef"] = {kk: float(f"{vv:.4g}") for kk, vv in f["coef"].items()}
+        f["r2"], f["max_rel_err"] = round(f["r2"], 4), round(f["max_rel_err"], 4)
+    return {"fits": fits, "policies": per_policy, "n_shards_timed": len(rows),
+            "rows": [[r["workload"][:12], r["policy"], r["pairs"], r["fwd_tiles"], r["fwd_qtiles"],
+                      r["bwd_tiles"], r["bwd_ktiles"], round(r["fwd_ms"], 4), round(r["bwd_ms"], 4)]
+                     for r in rows],
+            "note": "ms per shard launch (all SMs on one shard); counts over all heads; fits with a "
+                    "per-launch intercept over all timed shards"}
 
 
 def _bench_ring(s, q, k, v, w, pairs, torch, fcp):
@@ -485,7 +530,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=3.0)
     ap.add_argument("--legs", default="step,merge,ring,e2e,cpu",
-                    help="parts to run: step (always), merge, ring, e2e, cpu; e.g. 'step' for profiling")
+                    help="parts to run: step (always), merge, ring, shards, e2e, cpu; e.g. 'step' for "
+                         "profiling; 'shards' (per-shard calibration) is not in the default set")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "fcp":
         args.warmup = 3

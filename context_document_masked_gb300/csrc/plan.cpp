@@ -45,6 +45,26 @@ static int64_t sum_work(const std::vector<Piece>& ps, const std::vector<int32_t>
   return w;
 }
 
+// Kernel-unit cost of a shard (the hybrid_tiles policy): for each of its
+// ceil(s/128) query tiles, the ceil((p + e)/128) key tiles of the document's
+// causal prefix up to the tile's local end e, plus one per query tile -- the
+// tiles the attention kernels visit when the keys form one run from the
+// document start. Measured per-shard time on GB300 (forward + backward)
+// fits visited tiles and query tiles with equal weights.
+static int64_t tile_cost(int64_t p, int64_t s) {
+  const int64_t nq = (s + kTileM - 1) / kTileM;
+  int64_t c = nq;
+  for (int64_t t = 0; t < nq; ++t) c += (p + std::min<int64_t>(kTileM * (t + 1), s) + kTileN - 1) / kTileN;
+  return c;
+}
+
+static int64_t sum_cost(const std::vector<Piece>& ps, const std::vector<int32_t>& off, bool tiles) {
+  if (!tiles) return sum_work(ps, off);
+  int64_t w = 0;
+  for (const Piece& p : ps) w += tile_cost(p.start - off[p.doc], p.end - p.start);
+  return w;
+}
+
 static int64_t sum_tokens(const std::vector<Piece>& ps) {
   int64_t t = 0;
   for (const Piece& p : ps) t += p.end - p.start;
@@ -143,8 +163,9 @@ int Plan::build_perdoc() {
   return FCP_OK;
 }
 
-// Algorithm 1 of FlashCP (§3.4).
-int Plan::build_algorithm1(double R) {
+// Algorithm 1 of FlashCP (§3.4). `tiles`: a piece's workload is its kernel
+// tile cost instead of W (placement and imbalance alike).
+int Plan::build_algorithm1(double R, bool tiles) {
   if (T % N != 0) return FCP_ERR_INFEASIBLE;
   const int32_t n = (int32_t)D.size();
   const int64_t target_total = T / N;
@@ -163,7 +184,7 @@ int Plan::build_algorithm1(double R) {
     for (int32_t doc : pd_order) perdoc_pieces(doc, D[doc], off[doc], N, base);
     std::vector<int64_t> load(N), target(N), tokens(N, 0);
     for (int32_t j = 0; j < N; ++j) {
-      load[j] = sum_work(base[j], off);
+      load[j] = sum_cost(base[j], off, tiles);
       target[j] = target_total - sum_tokens(base[j]);
     }
     std::vector<int64_t> base_w = load;
@@ -175,7 +196,7 @@ int Plan::build_algorithm1(double R) {
       for (int32_t w = 1; w < N; ++w)
         if (load[w] < load[j]) j = w;
       tmp[j].push_back(Piece{doc, off[doc], off[doc] + D[doc]});
-      load[j] += piece_work(0, D[doc]);
+      load[j] += tiles ? tile_cost(0, D[doc]) : piece_work(0, D[doc]);
       tokens[j] += D[doc];
     }
     // Lines 11-16: equal-token repair with Whole-Doc sharding.
@@ -210,7 +231,7 @@ int Plan::build_algorithm1(double R) {
     // Line 18: imbalance of the complete plan.
     int64_t sumW = 0, maxW = 0;
     for (int32_t j = 0; j < N; ++j) {
-      int64_t w = base_w[j] + sum_work(tmp[j], off);
+      int64_t w = base_w[j] + sum_cost(tmp[j], off, tiles);
       sumW += w;
       maxW = std::max(maxW, w);
     }
@@ -239,8 +260,8 @@ int Plan::build_algorithm1(double R) {
 int make_plan(const int32_t* doclens, int32_t n_docs, int32_t cp, int32_t policy, double R,
               fcp_plan_t** out) {
   if (!doclens || !out || n_docs < 1 || cp < 1) return FCP_ERR_INVALID_ARG;
-  if (policy < FCP_POLICY_LLAMA3 || policy > FCP_POLICY_HYBRID) return FCP_ERR_INVALID_ARG;
-  if (policy == FCP_POLICY_HYBRID && !(R > 0)) return FCP_ERR_INVALID_ARG;
+  if (policy < FCP_POLICY_LLAMA3 || policy > FCP_POLICY_HYBRID_TILES) return FCP_ERR_INVALID_ARG;
+  if ((policy == FCP_POLICY_HYBRID || policy == FCP_POLICY_HYBRID_TILES) && !(R > 0)) return FCP_ERR_INVALID_ARG;
   fcp_plan_t* p = new fcp_plan_t();
   p->N = cp;
   p->D.assign(doclens, doclens + n_docs);
@@ -257,8 +278,9 @@ int make_plan(const int32_t* doclens, int32_t n_docs, int32_t cp, int32_t policy
   switch (policy) {
     case FCP_POLICY_LLAMA3: st = p->build_llama3(); break;
     case FCP_POLICY_PER_DOC: st = p->build_perdoc(); break;
-    case FCP_POLICY_WHOLE_DOC: st = p->build_algorithm1(std::numeric_limits<double>::infinity()); break;
-    default: st = p->build_algorithm1(R); break;
+    case FCP_POLICY_WHOLE_DOC: st = p->build_algorithm1(std::numeric_limits<double>::infinity(), false); break;
+    case FCP_POLICY_HYBRID_TILES: st = p->build_algorithm1(R, true); break;
+    default: st = p->build_algorithm1(R, false); break;
   }
   if (st != FCP_OK) { delete p; return st; }
   p->build_work_tables();

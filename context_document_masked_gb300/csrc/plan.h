@@ -65,7 +65,7 @@ struct Plan {
 
   int build_llama3();
   int build_perdoc();
-  int build_algorithm1(double R);
+  int build_algorithm1(double R, bool tiles);
   void finish(std::vector<std::vector<Piece>>& wp);
   void build_work_tables();
 };

@@ -15,7 +15,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libfcp.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_INFEASIBLE, ERR_CAPACITY = range(7)
-POLICIES = {"llama3": 0, "perdoc": 1, "wholedoc": 2, "hybrid": 3}
+POLICIES = {"llama3": 0, "perdoc": 1, "wholedoc": 2, "hybrid": 3, "hybrid_tiles": 4}
 OUT_BF16, OUT_F32 = 0, 1
 
 EXPORTED = (

@@ -50,7 +50,10 @@ enum {
   FCP_POLICY_LLAMA3 = 0,     /* [FlashCP] §2.2/§2.3: sequence in 2N chunks, i & 2N-1-i */
   FCP_POLICY_PER_DOC = 1,    /* [FlashCP] §2.3: every doc in 2N chunks, i & 2N-1-i    */
   FCP_POLICY_WHOLE_DOC = 2,  /* [FlashCP] Algorithm 1 with R = infinity               */
-  FCP_POLICY_HYBRID = 3      /* [FlashCP] Algorithm 1 with target imbalance R         */
+  FCP_POLICY_HYBRID = 3,     /* [FlashCP] Algorithm 1 with target imbalance R         */
+  FCP_POLICY_HYBRID_TILES = 4 /* Algorithm 1 with R, a piece's workload in kernel tiles:
+                                 sum over its query tiles of the key tiles of the causal
+                                 prefix, plus one per query tile (instead of W)        */
 };
 
 enum {
@@ -120,7 +123,8 @@ typedef struct {
  *   doclens  host int32[n_docs], each >= 1, sum = T (the packed sequence).
  *   cp       N >= 1 shards.
  *   policy   FCP_POLICY_*.
- *   target_imbalance  R for FCP_POLICY_HYBRID (ignored otherwise; > 0).
+ *   target_imbalance  R for FCP_POLICY_HYBRID / _HYBRID_TILES (ignored
+ *            otherwise; > 0). The plan's reported imbalance is always by W.
  *   out      receives a new plan, to be freed with fcp_plan_free.
  * Errors: FCP_ERR_INVALID_ARG (null, n_docs < 1, a length < 1, T >= 2^31),
  *         FCP_ERR_INFEASIBLE (Llama3 needs T % 2N == 0; Whole-Doc and hybrid

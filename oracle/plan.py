@@ -20,6 +20,15 @@ Policies:
            i and 2N-1-i. Chunk boundaries are floor(c L / 2N).
   wholedoc Algorithm 1 (§3.4) with the Per-Doc branch never taken (R = inf).
   hybrid   Algorithm 1 with target imbalance R.
+  hybrid_tiles  Algorithm 1 with target imbalance R, a piece's workload
+           measured in the attention kernels' own units instead of W: the
+           128 x 128 tiles its query rows touch in the document's causal
+           prefix (keys taken as one run from the document start) plus one
+           per query tile. The weights are those of a least-squares fit of
+           measured per-shard forward + backward time on GB300 against visited
+           tiles and query tiles, which came out equal. FlashCP §2.2 ("Reduced
+           Kernel Efficiency", Fig. 3) is the motivation: short shards cost
+           more per useful pair. The greedy placement and Cur_R both use it.
 
 Readings of Algorithm 1 where the text is open:
   * "least-loaded worker" (Min_Worker_Add) is by workload W, ties to the
@@ -54,7 +63,7 @@ from __future__ import annotations
 import dataclasses
 import math
 
-POLICIES = ("llama3", "perdoc", "wholedoc", "hybrid")
+POLICIES = ("llama3", "perdoc", "wholedoc", "hybrid", "hybrid_tiles")
 DEFAULT_R = 1.05
 
 
@@ -107,6 +116,18 @@ class Plan:
 def workload(p: int, s: int) -> int:
     """W_i = (2 p_i + s_i + 1) s_i / 2, exact in integers."""
     return (2 * p + s + 1) * s // 2
+
+
+TILE = 128
+
+
+def tile_cost(p: int, s: int) -> int:
+    """Kernel-unit cost of a shard of s tokens whose document prefix is p
+    tokens: for each of its ceil(s/128) query tiles, the ceil((p + e)/128) key
+    tiles of the causal prefix up to the tile's local end e, plus one per
+    query tile."""
+    nq = -(-s // TILE)
+    return sum(-(-(p + min(TILE * (t + 1), s)) // TILE) for t in range(nq)) + nq
 
 
 def _offsets(D):
@@ -219,9 +240,11 @@ def plan_perdoc(D, N: int) -> Plan:
     return _finish(N, T, D, offsets, wp, [1] * len(D), 1)
 
 
-def plan_algorithm1(D, N: int, R: float) -> Plan:
+def plan_algorithm1(D, N: int, R: float, cost=None) -> Plan:
     """Algorithm 1 of FlashCP (§3.4): Whole-Doc placement with Per-Doc for the
-    documents that keep the imbalance above R."""
+    documents that keep the imbalance above R. `cost(p, s)` measures a
+    piece's workload (default W)."""
+    cost = workload if cost is None else cost
     offsets, T = _offsets(D)
     n = len(D)
     if T % N != 0:
@@ -239,7 +262,7 @@ def plan_algorithm1(D, N: int, R: float) -> Plan:
         for doc in per_doc_P:
             for j, ps in enumerate(_perdoc_pieces(doc, D[doc], offsets[doc], N)):
                 base[j].extend(ps)
-        base_W = [sum(workload(p.start - offsets[p.doc], p.s) for p in ps) for ps in base]
+        base_W = [sum(cost(p.start - offsets[p.doc], p.s) for p in ps) for ps in base]
         base_tok = [sum(p.s for p in ps) for ps in base]
         target = [target_total - base_tok[j] for j in range(N)]
         # Lines 5-9: each remaining document goes whole to the least-loaded worker.
@@ -250,7 +273,7 @@ def plan_algorithm1(D, N: int, R: float) -> Plan:
                 continue
             j = min(range(N), key=lambda w: (load[w], w))
             tmp_P[j].append(Piece(doc, offsets[doc], offsets[doc] + D[doc]))
-            load[j] += workload(0, D[doc])
+            load[j] += cost(0, D[doc])
         # Lines 11-16: restore equal token counts (Eq. 2) with Whole-Doc sharding.
         tokens = [sum(p.s for p in ps) for ps in tmp_P]
         while True:
@@ -275,7 +298,7 @@ def plan_algorithm1(D, N: int, R: float) -> Plan:
             tokens[A] -= moved
             tokens[B] += moved
         # Line 18: imbalance of the complete plan.
-        Wj = [base_W[j] + sum(workload(p.start - offsets[p.doc], p.s) for p in tmp_P[j])
+        Wj = [base_W[j] + sum(cost(p.start - offsets[p.doc], p.s) for p in tmp_P[j])
               for j in range(N)]
         sumW = sum(Wj)
         cur_r = (max(Wj) / (sumW / N)) if sumW > 0 else 1.0
@@ -302,4 +325,6 @@ def make_plan(D, N: int, policy: str, R: float = DEFAULT_R) -> Plan:
         return plan_algorithm1(D, N, math.inf)
     if policy == "hybrid":
         return plan_algorithm1(D, N, R)
+    if policy == "hybrid_tiles":
+        return plan_algorithm1(D, N, R, cost=tile_cost)
     raise ValueError(policy)

@@ -135,6 +135,33 @@ def test_hybrid_meets_target_or_exhausts_documents():
         assert plan.imbalance <= 1.05 or all(plan.per_doc)
 
 
+@pytest.mark.parametrize("p,s", [(0, 1), (0, 128), (0, 129), (5, 1), (5, 300), (127, 2), (128, 128),
+                                 (200, 257), (1000, 31), (0, 700), (333, 513)])
+def test_tile_cost_counts_touched_tiles(p, s):
+    """hybrid_tiles cost of a shard: the (query tile, key tile) cells holding
+    at least one causal pair -- query tiles from the shard start, key tiles
+    from the document start -- enumerated pair by pair, plus its query tiles."""
+    cells = {((q - p) // 128, k // 128) for q in range(p, p + s) for k in range(q + 1)}
+    assert P.tile_cost(p, s) == len(cells) + -(-s // 128)
+
+
+def test_tile_cost_whole_document_closed_form():
+    for L in (1, 127, 128, 129, 4096, 8833):
+        n = -(-L // 128)
+        assert P.tile_cost(0, L) == n * (n + 1) // 2 + n
+
+
+def test_hybrid_tiles_meets_target_in_its_cost():
+    """Algorithm 1 with the tile cost stops once the cost imbalance is within
+    R, or after every document went Per-Doc."""
+    for cfg in (2, 3, 4):
+        D = synth.doc_lengths(cfg)
+        N = synth.WORKLOADS[cfg].cp
+        plan = P.make_plan(D, N, "hybrid_tiles", 1.05)
+        costs = [sum(P.tile_cost(pc.start - plan.offsets[pc.doc], pc.s) for pc in sh.pieces) for sh in plan.shards]
+        assert max(costs) / (sum(costs) / N) <= 1.05 or all(plan.per_doc)
+
+
 def test_wholedoc_cuts_communication():
     """Whole-Doc exchanges no more than Per-Doc on the skewed workloads (§3.2,
     Eq. 4 vs Eq. 5)."""
