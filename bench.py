@@ -380,8 +380,13 @@ def _bench_ring(s, q, k, v, w, pairs, torch, fcp):
             s.forward_ring(q, k, v, ring_step=st, out=o_parts[st], lse=l_parts[st])
         fcp.merge(o_parts, l_parts, mo, ml)
 
+    def gathered_qk8():
+        s.gather(k, v)
+        s.forward_qk8(q, k, v, out=out, lse=lse)
+
     res = {}
-    for name, fn in (("gather_then_forward", gathered), ("ring_fused", fused), ("ring_steps_then_merge", stepwise)):
+    for name, fn in (("gather_then_forward", gathered), ("ring_fused", fused), ("ring_steps_then_merge", stepwise),
+                     ("gather_then_forward_e4m3_qk", gathered_qk8)):
         for _ in range(3):
             fn()
         torch.cuda.synchronize()
@@ -396,7 +401,8 @@ def _bench_ring(s, q, k, v, w, pairs, torch, fcp):
         res[name] = {"ms": round(ms, 4), "tflops": round(4.0 * d * hq * pairs / (ms * 1e-3) / 1e12, 2)}
     if s.device_status() != 0:
         raise RuntimeError("device status reports a failed wait in the ring leg")
-    res["note"] = "useful fwd FLOPs / time; (c) includes the N partial forwards and the merge"
+    res["note"] = ("useful fwd FLOPs / time; (c) includes the N partial forwards and the merge; the e4m3 "
+                   "Q K^T form includes its per-call quantisation of Q, K and the received K rows")
     return res
 
 

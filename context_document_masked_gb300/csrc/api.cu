@@ -76,6 +76,20 @@ bool make_map_f32(CUtensorMap* m, void* ptr, int d, int heads, int64_t rows) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// e4m3 [rows][heads][d] tensor (one byte per element), boxes of d x 1 x 128
+// (d = 128: one 128-byte swizzled row per key or query).
+bool make_map_u8(CUtensorMap* m, void* ptr, int d, int heads, int64_t rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)d, (cuuint64_t)heads * d};
+  cuuint32_t box[3] = {(cuuint32_t)d, 1, 128};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, ptr, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 const int32_t* table(const fcp_dev_plan* dp, int tb) { return dp->base + dp->tables[tb]; }
@@ -226,8 +240,13 @@ int fcp_plan_upload(const fcp_plan_t* plan, void* dev_buf, int64_t bytes, void* 
 constexpr int64_t kWorkCounterOff = 64;
 
 struct WsLayout {
-  int64_t delta, q16, do16, v16, vb16, total;
+  int64_t delta, q16, do16, v16, vb16, q8, k8, kb8, total;
 };
+
+// Header words of the e4m3 Q K^T forward: amax bits of Q and K, then their
+// scales 2^kq and 2^kk.
+constexpr int64_t kQkAmaxOff = 128;
+constexpr int64_t kQkScaleOff = 136;
 
 static int64_t ws_align(int64_t x) { return (x + 255) / 256 * 256; }
 
@@ -240,7 +259,11 @@ static WsLayout ws_layout(const fcp_dims& d, int64_t remote_rows) {
   w.do16 = w.q16 + ws_align(T * hq * dd * 2);
   w.v16 = w.do16 + ws_align(T * hq * dd * 2);
   w.vb16 = w.v16 + ws_align(T * hkv * dd * 2);
-  w.total = w.vb16 + ws_align(std::max<int64_t>(remote_rows, 0) * hkv * dd * 2);
+  const int64_t R = std::max<int64_t>(remote_rows, 0);
+  w.q8 = w.vb16 + ws_align(R * hkv * dd * 2);
+  w.k8 = w.q8 + ws_align(T * hq * dd);
+  w.kb8 = w.k8 + ws_align(T * hkv * dd);
+  w.total = w.kb8 + ws_align(R * hkv * dd);
   return w;
 }
 
@@ -276,7 +299,7 @@ int fcp_gather_kv(const void* k, const void* v, const fcp_dev_plan* plan, int32_
 static int attn_fwd_impl(const void* q, const void* k, const void* v, const void* kbuf, const void* vbuf,
                          const fcp_dev_plan* plan, int32_t shard, int32_t kv_lo, int32_t kv_hi,
                          fcp_dims dims, int32_t out_dtype, void* out, float* lse, void* ws,
-                         int64_t ws_bytes, void* stream, int32_t ring) {
+                         int64_t ws_bytes, void* stream, int32_t ring, bool qk8 = false) {
   const bool ring_order = ring >= -1;
   int st = check_dev_plan(plan, shard);
   if (st) return st;
@@ -300,6 +323,22 @@ static int attn_fwd_impl(const void* q, const void* k, const void* v, const void
   void* v16 = wsb + wl.v16;
   void* vb16 = wsb + wl.vb16;
   int* counter = reinterpret_cast<int*>(wsb + kWorkCounterOff);
+  if (qk8) {
+    // e4m3 copies of Q, K and the received K rows (with K's scale: they are
+    // copies of K rows), each tensor with its own power-of-two scale.
+    if (dims.d != 128) return FCP_ERR_UNSUPPORTED;
+    unsigned* amax = reinterpret_cast<unsigned*>(wsb + kQkAmaxOff);
+    float* scales = reinterpret_cast<float*>(wsb + kQkScaleOff);
+    if (cudaMemsetAsync(amax, 0, 2 * sizeof(unsigned), cs) != cudaSuccess) return FCP_ERR_CUDA;
+    int sq = fcp::launch_quant_e4m3(q, wsb + wl.q8, (int64_t)dims.T * dims.hq * dims.d, amax, scales,
+                                    num_sms(), cs);
+    if (sq == FCP_OK)
+      sq = fcp::launch_quant_e4m3(k, wsb + wl.k8, (int64_t)dims.T * dims.hkv * dims.d, amax + 1, scales + 1,
+                                  num_sms(), cs);
+    if (sq == FCP_OK && rrows > 0)
+      sq = fcp::launch_quant_e4m3_with(kbuf, wsb + wl.kb8, rrows * dims.hkv * dims.d, amax + 1, num_sms(), cs);
+    if (sq) return sq;
+  }
   int st2 = fcp::launch_convert_f16(v, v16, (int64_t)dims.T * dims.hkv * dims.d, static_cast<int*>(ws),
                                     counter, num_sms(), cs);
   if (st2 == FCP_OK && rrows > 0)
@@ -309,14 +348,18 @@ static int attn_fwd_impl(const void* q, const void* k, const void* v, const void
 
   fcp::FwdLaunch a;
   std::memset(&a, 0, sizeof(a));
-  bool ok = make_map(&a.tm_q, q, dims.d, dims.hq, dims.T) && make_map(&a.tm_k, k, dims.d, dims.hkv, dims.T) &&
-            make_map(&a.tm_v, v16, dims.d, dims.hkv, dims.T, true);
-  if (rrows > 0)
-    ok = ok && make_map(&a.tm_kb, kbuf, dims.d, dims.hkv, rrows) &&
-         make_map(&a.tm_vb, vb16, dims.d, dims.hkv, rrows, true);
-  else
-    ok = ok && make_map(&a.tm_kb, k, dims.d, dims.hkv, dims.T) && make_map(&a.tm_vb, v16, dims.d, dims.hkv, dims.T, true);
+  bool ok = make_map(&a.tm_v, v16, dims.d, dims.hkv, dims.T, true);
+  if (qk8) {
+    ok = ok && make_map_u8(&a.tm_q, wsb + wl.q8, dims.d, dims.hq, dims.T) &&
+         make_map_u8(&a.tm_k, wsb + wl.k8, dims.d, dims.hkv, dims.T) &&
+         make_map_u8(&a.tm_kb, rrows > 0 ? wsb + wl.kb8 : wsb + wl.k8, dims.d, dims.hkv, rrows > 0 ? rrows : dims.T);
+  } else {
+    ok = ok && make_map(&a.tm_q, q, dims.d, dims.hq, dims.T) && make_map(&a.tm_k, k, dims.d, dims.hkv, dims.T) &&
+         make_map(&a.tm_kb, rrows > 0 ? kbuf : k, dims.d, dims.hkv, rrows > 0 ? rrows : dims.T);
+  }
+  ok = ok && make_map(&a.tm_vb, rrows > 0 ? vb16 : v16, dims.d, dims.hkv, rrows > 0 ? rrows : dims.T, true);
   if (!ok) return FCP_ERR_CUDA;
+  a.qk8 = qk8;
   fcp::FwdParams& fp = a.p;
   fp.pieces = table(plan, ring_order ? fcp::TB_RPIECES : fcp::TB_PIECES);
   fp.segs = table(plan, ring_order ? fcp::TB_RSEGS : fcp::TB_SEGS);
@@ -343,6 +386,7 @@ static int attn_fwd_impl(const void* q, const void* k, const void* v, const void
   fp.lse = lse;
   fp.err = static_cast<int*>(ws);
   fp.work_counter = counter;
+  fp.qk_scale = qk8 ? reinterpret_cast<const float*>(wsb + kQkScaleOff) : nullptr;
   fp.wait_ns = g_wait_ns;
   a.d = dims.d;
   a.num_sms = num_sms();
@@ -355,6 +399,24 @@ int fcp_attn_fwd(const void* q, const void* k, const void* v, const void* kbuf, 
                  int64_t ws_bytes, void* stream) {
   return attn_fwd_impl(q, k, v, kbuf, vbuf, plan, shard, kv_lo, kv_hi, dims, out_dtype, out, lse, ws,
                        ws_bytes, stream, -2);
+}
+
+int fcp_attn_fwd_qk8(const void* q, const void* k, const void* v, const void* kbuf, const void* vbuf,
+                     const fcp_dev_plan* plan, int32_t shard, int32_t kv_lo, int32_t kv_hi, fcp_dims dims,
+                     int32_t out_dtype, void* out, float* lse, void* ws, int64_t ws_bytes, void* stream) {
+  return attn_fwd_impl(q, k, v, kbuf, vbuf, plan, shard, kv_lo, kv_hi, dims, out_dtype, out, lse, ws,
+                       ws_bytes, stream, -2, true);
+}
+
+int fcp_quant_e4m3(const void* x, int64_t n, void* out, float* scale_out, void* scratch, void* stream) {
+  if (n < 0 || n % 8 != 0) return FCP_ERR_INVALID_ARG;
+  if (n == 0) return FCP_OK;
+  if (!x || !out || !scale_out || !scratch) return FCP_ERR_INVALID_ARG;
+  if (!aligned16(x) || (reinterpret_cast<uintptr_t>(out) & 7) || (reinterpret_cast<uintptr_t>(scratch) & 3))
+    return FCP_ERR_INVALID_ARG;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(scratch, 0, sizeof(unsigned), cs) != cudaSuccess) return FCP_ERR_CUDA;
+  return fcp::launch_quant_e4m3(x, out, n, static_cast<unsigned*>(scratch), scale_out, num_sms(), cs);
 }
 
 int fcp_attn_fwd_ring(const void* q, const void* k, const void* v, const fcp_dev_plan* plan,

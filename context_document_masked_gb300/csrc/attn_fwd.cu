@@ -140,7 +140,7 @@ __device__ __forceinline__ WorkItem decode(const FwdParams& p, int w) {
   return it;
 }
 
-template <int D>
+template <int D, bool QK8>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kb,
@@ -214,11 +214,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nt = count_key_tiles(p.segs, it.seg_begin, it.seg_count, q_last, p.kv_lo, p.kv_hi, p.seg_filter);
         if (nt == 0) continue;
         if (q_iter > 0 && !(ok = mbar_wait_inline(&bar_q_empty, (q_iter - 1) & 1, wc))) break;
-        mbar_arrive_expect_tx(&bar_q_full, 2 * C::kTileBytes);
-        for (int h = 0; h < 2; ++h)
-          for (int pn = 0; pn < C::kPanels; ++pn)
-            tma_load_3d(sQ + h * C::kTileBytes + pn * 16384, &tm_q, &bar_q_full, pn * 64, it.h0 + h,
-                        it.q_start);
+        if constexpr (QK8) {  // e4m3 rows of D bytes: one box per head
+          mbar_arrive_expect_tx(&bar_q_full, 2 * 128 * D);
+          for (int h = 0; h < 2; ++h)
+            tma_load_3d(sQ + h * C::kTileBytes, &tm_q, &bar_q_full, 0, it.h0 + h, it.q_start);
+        } else {
+          mbar_arrive_expect_tx(&bar_q_full, 2 * C::kTileBytes);
+          for (int h = 0; h < 2; ++h)
+            for (int pn = 0; pn < C::kPanels; ++pn)
+              tma_load_3d(sQ + h * C::kTileBytes + pn * 16384, &tm_q, &bar_q_full, pn * 64, it.h0 + h,
+                          it.q_start);
+        }
         ++q_iter;
         Walker wk;
         wk.init(p.segs, it.seg_begin, it.seg_count, q_last, p.kv_lo, p.kv_hi, p.kbuf_shift, p.seg_filter);
@@ -229,11 +235,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (kv_cnt >= (uint32_t)C::kStages &&
                 !(ok = mbar_wait_inline(&bar_kv_empty[s], ((kv_cnt / C::kStages) - 1) & 1, wc)))
               break;
-            mbar_arrive_expect_tx(&bar_kv_full[s], C::kTileBytes);
             const CUtensorMap* tm = kv == 0 ? (src ? &tm_kb : &tm_k) : (src ? &tm_vb : &tm_v);
-            for (int pn = 0; pn < C::kPanels; ++pn)
-              tma_load_3d(sKV + s * C::kTileBytes + pn * 16384, tm, &bar_kv_full[s], pn * 64, it.g,
-                          row);
+            if (QK8 && kv == 0) {  // e4m3 K tile: one box of D-byte rows
+              mbar_arrive_expect_tx(&bar_kv_full[s], 128 * D);
+              tma_load_3d(sKV + s * C::kTileBytes, tm, &bar_kv_full[s], 0, it.g, row);
+            } else {
+              mbar_arrive_expect_tx(&bar_kv_full[s], C::kTileBytes);
+              for (int pn = 0; pn < C::kPanels; ++pn)
+                tma_load_3d(sKV + s * C::kTileBytes + pn * 16384, tm, &bar_kv_full[s], pn * 64, it.g,
+                            row);
+            }
             ++issued[s];
             ++kv_cnt;
           }
@@ -247,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idesc_s = QK8 ? idesc_e4m3_f32(128, 128) : idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idesc_o = idesc_f16kind(128, D, false, true, false);  // fp16 P, V
       uint32_t kv_cnt = 0, q_iter = 0, items = 0;
       uint32_t p_cnt[2] = {0, 0};
@@ -257,11 +268,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_s = [&](int i, uint32_t kstage) {
         const uint32_t qa = q_base + i * C::kTileBytes;
         const uint32_t ka = kv_base + kstage * C::kTileBytes;
+        if constexpr (QK8) {  // K steps of 32 e4m3 values (32 bytes) along one 128-byte row
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_bf16_ss(tmem + C::kColS + i * 128, smem_desc_sw128(qa + off, 0, 1024),
-                      smem_desc_sw128(ka + off, 0, 1024), idesc_s, kk > 0);
+          for (int kk = 0; kk < D / 32; ++kk)
+            mma_f8_ss(tmem + C::kColS + i * 128, smem_desc_sw128(qa + kk * 32, 0, 1024),
+                      smem_desc_sw128(ka + kk * 32, 0, 1024), idesc_s, kk > 0);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_bf16_ss(tmem + C::kColS + i * 128, smem_desc_sw128(qa + off, 0, 1024),
+                        smem_desc_sw128(ka + off, 0, 1024), idesc_s, kk > 0);
+          }
         }
       };
       auto issue_o = [&](int i, uint32_t vstage, bool acc) {
@@ -339,6 +357,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t s_cnt = 0, o_cnt = 0;
     bool ok = true;
     const bool out_v8 = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
+    // e4m3 Q K^T: S comes out scaled by 2^kq 2^kk (powers of two, exact).
+    const float scale_log2 = QK8 ? p.scale_log2 / (p.qk_scale[0] * p.qk_scale[1]) : p.scale_log2;
     for (uint32_t k = 0; ok; ++k) {
       int w = 0;
       ok = ring.get<true>(k, w, wc);
@@ -389,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mx8[j] = m;
           }
           const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], fmax3(mx8[5], mx8[6], mx8[7]))) *
-                           p.scale_log2;
+                           scale_log2;
           const float m_new = fmaxf(m_run, mx);
           const bool rescale = m_new > m_run + kRescaleThreshold;
           float alpha = 1.f;
@@ -401,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // P = exp2(s * scale * log2e - m): fp16 pairs straight into TMEM columns
           // [0, 64) of S_i, 64 score columns at a time. The scaling and the row
           // sum run on packed pairs; sums of column c go to accumulator c mod 8.
-          const uint64_t c2 = f2(p.scale_log2, p.scale_log2), nm2 = f2(-m_use, -m_use);
+          const uint64_t c2 = f2(scale_log2, scale_log2), nm2 = f2(-m_use, -m_use);
           uint64_t rs2[4] = {0, 0, 0, 0};
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {  // 32 score columns -> 16 TMEM columns of P
@@ -510,14 +530,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-template <int D>
+template <int D, bool QK8>
 static int launch_fwd_impl(const FwdLaunch& a, cudaStream_t st) {
   using C = FwdCfg<D>;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(attn_fwd_kernel<D, QK8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemAlloc) != cudaSuccess)
       return FCP_ERR_CUDA;
     attr_set[dev] = true;
@@ -525,14 +545,15 @@ static int launch_fwd_impl(const FwdLaunch& a, cudaStream_t st) {
   const int n_work = a.p.n_items * (a.p.hq / 2);
   if (n_work == 0) return FCP_OK;
   const int grid = n_work < a.num_sms ? n_work : a.num_sms;
-  attn_fwd_kernel<D><<<grid, kThreads, C::kSmemAlloc, st>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_kb, a.tm_vb,
-                                                           a.p);
+  attn_fwd_kernel<D, QK8><<<grid, kThreads, C::kSmemAlloc, st>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_kb, a.tm_vb,
+                                                                a.p);
   return cudaGetLastError() == cudaSuccess ? FCP_OK : FCP_ERR_CUDA;
 }
 
 int launch_attn_fwd(const FwdLaunch& a, cudaStream_t st) {
-  if (a.d == 128) return launch_fwd_impl<128>(a, st);
-  if (a.d == 64) return launch_fwd_impl<64>(a, st);
+  if (a.qk8) return a.d == 128 ? launch_fwd_impl<128, true>(a, st) : FCP_ERR_UNSUPPORTED;
+  if (a.d == 128) return launch_fwd_impl<128, false>(a, st);
+  if (a.d == 64) return launch_fwd_impl<64, false>(a, st);
   return FCP_ERR_UNSUPPORTED;
 }
 

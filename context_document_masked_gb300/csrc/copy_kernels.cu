@@ -263,7 +263,86 @@ __global__ void __launch_bounds__(kCvtThreads)
   if (ovf) atomicOr(err, 4);
 }
 
+// ------------------------------------------------------- e4m3 quantisation
+// Per-tensor power-of-two scale 2^k, the largest with max|x| * 2^k <= 448
+// (the largest finite e4m3 value), so scaling and dequantising are exact;
+// rounding to nearest, ties to even, saturating (cvt .rn.satfinite).
+constexpr int kQuantThreads = 256;
+
+__global__ void __launch_bounds__(kQuantThreads)
+    amax_kernel(const uint4* __restrict__ x, int64_t n, unsigned* __restrict__ amax_bits) {
+  float m = 0.f;
+  for (int64_t i = (int64_t)blockIdx.x * kQuantThreads + threadIdx.x; i < n; i += (int64_t)gridDim.x * kQuantThreads) {
+    const uint4 v = __ldg(x + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[j] << 16)), fabsf(__uint_as_float(w[j] & 0xFFFF0000u))));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if ((threadIdx.x & 31) == 0) atomicMax(amax_bits, __float_as_uint(m));  // m >= 0: bits order as values
+}
+
+// 2^k from the bits of amax = (1 + f) 2^e: k = (f <= 0.75 ? 8 : 7) - e.
+__device__ __forceinline__ float e4m3_scale(unsigned amax_bits) {
+  if (amax_bits == 0) return 1.f;
+  const int e = (int)((amax_bits >> 23) & 0xFFu) - 127;
+  int k = ((amax_bits & 0x7FFFFFu) <= 0x600000u ? 8 : 7) - e;
+  k = max(-126, min(127, k));
+  return __uint_as_float((uint32_t)(k + 127) << 23);
+}
+
+// Four floats to four e4m3 bytes, a at the lowest address.
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+  uint16_t lo, hi;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+  return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+__global__ void __launch_bounds__(kQuantThreads)
+    quant_kernel(const uint4* __restrict__ x, uint2* __restrict__ y, int64_t n,
+                 const unsigned* __restrict__ amax_bits, float* __restrict__ scale_out) {
+  const float s = e4m3_scale(*amax_bits);
+  if (scale_out && blockIdx.x == 0 && threadIdx.x == 0) *scale_out = s;
+  for (int64_t i = (int64_t)blockIdx.x * kQuantThreads + threadIdx.x; i < n; i += (int64_t)gridDim.x * kQuantThreads) {
+    const uint4 v = __ldg(x + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float f[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      f[2 * j] = __uint_as_float(w[j] << 16) * s;
+      f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u) * s;
+    }
+    y[i] = make_uint2(e4m3x4(f[0], f[1], f[2], f[3]), e4m3x4(f[4], f[5], f[6], f[7]));
+  }
+}
+
 }  // namespace
+
+int launch_quant_e4m3(const void* src, void* dst, int64_t n_elems, unsigned* amax_bits, float* scale_out,
+                      int num_sms, cudaStream_t st) {
+  const int64_t n = n_elems / 8;
+  int64_t grid = (n + kQuantThreads - 1) / kQuantThreads;
+  if (grid > (int64_t)num_sms * 8) grid = (int64_t)num_sms * 8;
+  if (grid < 1) grid = 1;
+  amax_kernel<<<(int)grid, kQuantThreads, 0, st>>>(static_cast<const uint4*>(src), n, amax_bits);
+  quant_kernel<<<(int)grid, kQuantThreads, 0, st>>>(static_cast<const uint4*>(src), static_cast<uint2*>(dst), n,
+                                                    amax_bits, scale_out);
+  return cudaGetLastError() == cudaSuccess ? FCP_OK : FCP_ERR_CUDA;
+}
+
+int launch_quant_e4m3_with(const void* src, void* dst, int64_t n_elems, const unsigned* amax_bits,
+                           int num_sms, cudaStream_t st) {
+  const int64_t n = n_elems / 8;
+  if (n == 0) return FCP_OK;
+  int64_t grid = (n + kQuantThreads - 1) / kQuantThreads;
+  if (grid > (int64_t)num_sms * 8) grid = (int64_t)num_sms * 8;
+  quant_kernel<<<(int)grid, kQuantThreads, 0, st>>>(static_cast<const uint4*>(src), static_cast<uint2*>(dst), n,
+                                                    amax_bits, nullptr);
+  return cudaGetLastError() == cudaSuccess ? FCP_OK : FCP_ERR_CUDA;
+}
 
 int launch_convert_f16(const void* src, void* dst, int64_t n_elems, int* err, int* zero_word,
                        int num_sms, cudaStream_t st) {

@@ -25,6 +25,7 @@ struct FwdParams {
   float* lse;
   int* err;
   int* work_counter;       // zero at launch (set by the preceding kernel of the call)
+  const float* qk_scale;   // e4m3 Q K^T variant: the scales 2^kq, 2^kk of Q and K (else unused)
   int64_t wait_ns;
 };
 
@@ -33,6 +34,7 @@ struct FwdLaunch {
   FwdParams p;
   int d;
   int num_sms;
+  bool qk8;                // Q, K, received K as e4m3 (boxes of 128 bytes x 1 x 128)
 };
 
 struct BwdParams {
@@ -80,6 +82,17 @@ int launch_bwd_preprocess(const void* out, bool out_f32, const void* dout, const
 // (if not null) is set to 0, as above.
 int launch_convert_f16(const void* src, void* dst, int64_t n_elems, int* err, int* zero_word,
                        int num_sms, cudaStream_t st);
+
+// e4m3 copy of a bf16 array of n_elems (a multiple of 8) elements, scaled by
+// the power of two 2^k, the largest with max|x| * 2^k <= 448 (exact to undo).
+// *amax_bits must be zero on entry (it receives the bits of max|x|); the
+// scale goes to *scale_out.
+int launch_quant_e4m3(const void* src, void* dst, int64_t n_elems, unsigned* amax_bits,
+                      float* scale_out, int num_sms, cudaStream_t st);
+// The same with a scale computed before (from *amax_bits of another tensor):
+// rows copied from that tensor share its scale.
+int launch_quant_e4m3_with(const void* src, void* dst, int64_t n_elems, const unsigned* amax_bits,
+                           int num_sms, cudaStream_t st);
 
 // Gather of received KV rows: tasks (src_row, dst_row, nrows, shard).
 int launch_gather(const void* k, const void* v, const int32_t* tasks, int32_t n_tasks,

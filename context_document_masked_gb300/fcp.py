@@ -23,6 +23,7 @@ EXPORTED = (
     "fcp_plan_stats", "fcp_plan_per_doc_flags", "fcp_plan_device_bytes", "fcp_plan_upload",
     "fcp_workspace_bytes", "fcp_gather_kv", "fcp_attn_fwd", "fcp_merge", "fcp_attn_bwd",
     "fcp_get_device_status", "fcp_debug_set_wait_limit", "fcp_attn_fwd_noalloc", "fcp_attn_fwd_ring",
+    "fcp_attn_fwd_qk8", "fcp_quant_e4m3",
 )
 
 
@@ -90,6 +91,9 @@ def _load():
                                    vp, vp, vp, i64, vp]),
         "fcp_attn_fwd_ring": (C.c_int, [vp, vp, vp, C.POINTER(DevPlan), i32, i32, Dims, i32, vp, vp, vp, i64,
                                         vp]),
+        "fcp_attn_fwd_qk8": (C.c_int, [vp, vp, vp, vp, vp, C.POINTER(DevPlan), i32, i32, i32, Dims, i32,
+                                       vp, vp, vp, i64, vp]),
+        "fcp_quant_e4m3": (C.c_int, [vp, i64, vp, vp, vp, vp]),
         "fcp_merge": (C.c_int, [vp, vp, i32, i64, i32, i32, vp, vp, vp]),
         "fcp_attn_bwd": (C.c_int, [vp, vp, vp, vp, vp, vp, i32, vp, vp, C.POINTER(DevPlan), i32,
                                    Dims, vp, vp, vp, vp, i64, vp]),
@@ -243,6 +247,25 @@ def attn_fwd(q, k, v, kbuf, vbuf, dplan: DevicePlan, shard: int, out, lse, ws, k
                              shard, kv_lo, T if kv_hi is None else kv_hi, dm, out_dtype, _ptr(out),
                              _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
            "fcp_attn_fwd")
+
+
+def attn_fwd_qk8(q, k, v, kbuf, vbuf, dplan: DevicePlan, shard: int, out, lse, ws, kv_lo: int = 0,
+                 kv_hi: int | None = None, scale: float = 0.0, stream=None):
+    """fcp_attn_fwd_qk8: the forward with Q K^T on e4m3 copies of Q and K."""
+    import torch
+    T, hq, d = q.shape
+    dm = Dims(T, hq, k.shape[1], d, scale)
+    out_dtype = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
+    _check(_lib.fcp_attn_fwd_qk8(_ptr(q), _ptr(k), _ptr(v), _ptr(kbuf), _ptr(vbuf), C.byref(dplan.c),
+                                 shard, kv_lo, T if kv_hi is None else kv_hi, dm, out_dtype, _ptr(out),
+                                 _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "fcp_attn_fwd_qk8")
+
+
+def quant_e4m3(x, out, scale_out, scratch, stream=None):
+    """fcp_quant_e4m3: out (uint8, x.numel() bytes) = e4m3(x * 2^k); scale_out[0] = 2^k."""
+    _check(_lib.fcp_quant_e4m3(_ptr(x), x.numel(), _ptr(out), _ptr(scale_out), _ptr(scratch), _stream(stream)),
+           "fcp_quant_e4m3")
 
 
 def attn_fwd_ring(q, k, v, dplan: DevicePlan, shard: int, ring_step: int, out, lse, ws, scale: float = 0.0,

@@ -46,6 +46,18 @@ class CPAttention:
                      kv_lo=lo, kv_hi=hi, scale=self.scale, stream=stream)
         return out, lse
 
+    def forward_qk8(self, q, k, v, shard: int = -1, out=None, lse=None, kv_block=None,
+                    out_dtype=torch.bfloat16, stream=None):
+        """forward() with Q K^T on e4m3 copies of Q and K (d = 128)."""
+        if out is None:
+            out = torch.empty(self.T, self.hq, self.d, dtype=out_dtype, device=self.device)
+        if lse is None:
+            lse = torch.empty(self.hq, self.T, dtype=torch.float32, device=self.device)
+        lo, hi = (0, self.T) if kv_block is None else kv_block
+        fcp.attn_fwd_qk8(q, k, v, self.kbuf, self.vbuf, self.dplan, shard, out, lse, self.ws,
+                         kv_lo=lo, kv_hi=hi, scale=self.scale, stream=stream)
+        return out, lse
+
     def forward_ring(self, q, k, v, ring_step: int = -1, shard: int = -1, out=None, lse=None,
                      out_dtype=torch.bfloat16, stream=None):
         """Forward in ring order without the gathered buffer: ring_step -1 visits

@@ -192,7 +192,8 @@ typedef struct {
 } fcp_dims;
 
 /* Workspace the device calls on `plan` need, in bytes: an error word and the
- * attention kernels' work counter (set by each call before use), the
+ * attention kernels' work counter (set by each call before use), e4m3 copies
+ * of Q, K and the received K rows with their scales (fcp_attn_fwd_qk8), the
  * backward's row statistics D_i = <dO_i, O_i> ([Hq][T] fp32), fp16 copies of
  * Q and dO ([T][Hq][d] each, the backward's tensor-core operands) and of V and
  * the plan's received V rows (the forward's P*V operands). Calls that share a
@@ -233,6 +234,32 @@ int fcp_attn_fwd(const void* q, const void* k, const void* v, const void* kbuf,
                  const void* vbuf, const fcp_dev_plan* plan, int32_t shard,
                  int32_t kv_lo, int32_t kv_hi, fcp_dims dims, int32_t out_dtype,
                  void* out, float* lse, void* ws, int64_t ws_bytes, void* stream);
+
+/*
+ * fcp_quant_e4m3 -- FP8 (OCP E4M3) copy of a bf16 array with one
+ * power-of-two scale ("LLM Context Parallel in Production" lists FP8 among
+ * the precisions of CP attention): out[i] = e4m3(x[i] * 2^k), k the largest
+ * integer with max|x| * 2^k <= 448, rounded to nearest (ties to even) and
+ * saturated to +-448; *scale_out = 2^k (device float). Scaling by a power of
+ * two is exact, so out[i] / 2^k is the dequantised value.
+ *   n        elements, a multiple of 8; x 16-byte aligned, out 8-byte aligned.
+ *   scratch  4 bytes of device memory (4-byte aligned) for max|x|.
+ */
+int fcp_quant_e4m3(const void* x, int64_t n, void* out, float* scale_out, void* scratch, void* stream);
+
+/*
+ * fcp_attn_fwd_qk8 -- fcp_attn_fwd with the scores Q K^T computed on e4m3
+ * copies of Q, K and the received K rows (fcp_quant_e4m3: Q with its own
+ * scale, K and its received rows with K's), the product unscaled exactly
+ * in the softmax; P V runs on fp16 operands as in fcp_attn_fwd. d = 128 only
+ * (FCP_ERR_UNSUPPORTED otherwise). Arguments and results as fcp_attn_fwd;
+ * the workspace (same size) holds the e4m3 copies. The result is the
+ * attention of the dequantised Q and K with V.
+ */
+int fcp_attn_fwd_qk8(const void* q, const void* k, const void* v, const void* kbuf,
+                     const void* vbuf, const fcp_dev_plan* plan, int32_t shard,
+                     int32_t kv_lo, int32_t kv_hi, fcp_dims dims, int32_t out_dtype,
+                     void* out, float* lse, void* ws, int64_t ws_bytes, void* stream);
 
 /*
  * fcp_attn_fwd_ring -- the same forward in ring order, without a gathered
