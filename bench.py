@@ -35,7 +35,7 @@ UNIT = "TFLOP/s"
 
 # DRAM bytes of one backward call (preprocess + main kernel) on this workload,
 # from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum of both
-# kernels; profiles/attn_fwd_bwd_packed32k_h32kv8_d128_cp4_perdoc.md). Valid
+# kernels; the capture is summarised under profiles/). Valid
 # only for the code it was taken on: the backward's kernels and helpers, and
 # the parts of the launch code and parameters that set the backward up.
 # Reported as null once any of them changes.
