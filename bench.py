@@ -46,7 +46,7 @@ BWD_TRAFFIC = {
                 ("context_document_masked_gb300/csrc/kernels.h", "struct BwdParams", "int launch_attn_fwd"),
                 ("context_document_masked_gb300/csrc/api.cu", "int fcp_attn_bwd(", "int fcp_get_device_status(")],
     "sha256": "09282f80d276c867466409326a09f7fe7a7273cbb923f9cfa7b4bd8f3392d242",
-    "bytes": (2.776394 + 1.469725 + 1.087365 + 1.044097) * 1e9,
+    "bytes": (2.770413 + 1.460449 + 1.087052 + 1.043919) * 1e9,
 }
 
 
