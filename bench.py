@@ -45,7 +45,7 @@ BWD_TRAFFIC = {
                 ("context_document_masked_gb300/csrc/sm103.cuh", None, None),
                 ("context_document_masked_gb300/csrc/kernels.h", "struct BwdParams", "int launch_attn_fwd"),
                 ("context_document_masked_gb300/csrc/api.cu", "int fcp_attn_bwd(", "int fcp_get_device_status(")],
-    "sha256": "09282f80d276c867466409326a09f7fe7a7273cbb923f9cfa7b4bd8f3392d242",
+    "sha256": "328425bf80861f4a62b08bc2b54374ac04eefacfa75df7920900a9b2b934b9c8",
     "bytes": (2.770413 + 1.460449 + 1.087052 + 1.043919) * 1e9,
 }
 
