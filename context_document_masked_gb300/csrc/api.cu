@@ -209,15 +209,19 @@ int64_t fcp_plan_device_bytes(const fcp_plan_t* plan) {
   return plan ? (int64_t)plan->dev.size() * 4 : 0;
 }
 
-int fcp_plan_upload(const fcp_plan_t* plan, void* dev_buf, int64_t bytes, void* stream,
-                    fcp_dev_plan* out) {
+int fcp_plan_device_image(const fcp_plan_t* plan, void* dst, int64_t bytes) {
+  if (!plan || !dst) return FCP_ERR_INVALID_ARG;
+  const int64_t need = fcp_plan_device_bytes(plan);
+  if (bytes < need) return FCP_ERR_CAPACITY;
+  std::memcpy(dst, plan->dev.data(), (size_t)need);
+  return FCP_OK;
+}
+
+int fcp_plan_bind(const fcp_plan_t* plan, const void* dev_buf, int64_t bytes, fcp_dev_plan* out) {
   if (!plan || !dev_buf || !out) return FCP_ERR_INVALID_ARG;
   if (!aligned16(dev_buf)) return FCP_ERR_INVALID_ARG;
   const int64_t need = fcp_plan_device_bytes(plan);
   if (bytes < need) return FCP_ERR_CAPACITY;
-  if (cudaMemcpyAsync(dev_buf, plan->dev.data(), need, cudaMemcpyHostToDevice,
-                      static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return FCP_ERR_CUDA;
   std::memset(out, 0, sizeof(*out));
   out->host = plan;
   out->base = static_cast<const int32_t*>(dev_buf);
@@ -229,6 +233,16 @@ int fcp_plan_upload(const fcp_plan_t* plan, void* dev_buf, int64_t bytes, void* 
     out->tables[t] = plan->tab_off[t];
     out->counts[t] = plan->tab_cnt[t];
   }
+  return FCP_OK;
+}
+
+int fcp_plan_upload(const fcp_plan_t* plan, void* dev_buf, int64_t bytes, void* stream,
+                    fcp_dev_plan* out) {
+  const int st = fcp_plan_bind(plan, dev_buf, bytes, out);
+  if (st != FCP_OK) return st;
+  if (cudaMemcpyAsync(dev_buf, plan->dev.data(), (size_t)out->bytes, cudaMemcpyHostToDevice,
+                      static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FCP_ERR_CUDA;
   return FCP_OK;
 }
 

@@ -23,7 +23,7 @@ EXPORTED = (
     "fcp_plan_stats", "fcp_plan_per_doc_flags", "fcp_plan_device_bytes", "fcp_plan_upload",
     "fcp_workspace_bytes", "fcp_gather_kv", "fcp_attn_fwd", "fcp_merge", "fcp_attn_bwd",
     "fcp_get_device_status", "fcp_debug_set_wait_limit", "fcp_attn_fwd_noalloc", "fcp_attn_fwd_ring",
-    "fcp_attn_fwd_qk8", "fcp_quant_e4m3",
+    "fcp_attn_fwd_qk8", "fcp_quant_e4m3", "fcp_plan_device_image", "fcp_plan_bind",
 )
 
 
@@ -85,6 +85,8 @@ def _load():
         "fcp_plan_per_doc_flags": (C.c_int, [vp, C.POINTER(C.c_int32), i32]),
         "fcp_plan_device_bytes": (i64, [vp]),
         "fcp_plan_upload": (C.c_int, [vp, vp, i64, vp, C.POINTER(DevPlan)]),
+        "fcp_plan_device_image": (C.c_int, [vp, vp, i64]),
+        "fcp_plan_bind": (C.c_int, [vp, vp, i64, C.POINTER(DevPlan)]),
         "fcp_workspace_bytes": (i64, [Dims, vp]),
         "fcp_gather_kv": (C.c_int, [vp, vp, C.POINTER(DevPlan), i32, i32, i32, vp, vp, vp]),
         "fcp_attn_fwd": (C.c_int, [vp, vp, vp, vp, vp, C.POINTER(DevPlan), i32, i32, i32, Dims, i32,
@@ -183,13 +185,39 @@ class Plan:
     def device_bytes(self) -> int:
         return int(_lib.fcp_plan_device_bytes(self._ptr))
 
-    def upload(self, buf, stream=None) -> "DevicePlan":
-        """Copy the work tables into `buf` (a device tensor of >= device_bytes())."""
+    def device_image(self) -> np.ndarray:
+        """The work tables as fcp_plan_upload would send them (int32 words)."""
+        out = np.empty(self.device_bytes() // 4, dtype=np.int32)
+        _check(_lib.fcp_plan_device_image(self._ptr, out.ctypes.data_as(C.c_void_p), out.nbytes),
+               "fcp_plan_device_image")
+        return out
+
+    def bind(self, buf) -> "DevicePlan":
+        """Handle for a device tensor that holds (or is about to hold) the image."""
         dp = DevPlan()
-        _check(_lib.fcp_plan_upload(self._ptr, C.c_void_p(buf.data_ptr()),
-                                    buf.numel() * buf.element_size(), _stream(stream), C.byref(dp)),
-               "fcp_plan_upload")
+        _check(_lib.fcp_plan_bind(self._ptr, C.c_void_p(buf.data_ptr()), buf.numel() * buf.element_size(),
+                                  C.byref(dp)), "fcp_plan_bind")
         return DevicePlan(dp, self, buf)
+
+    def upload(self, buf, stream=None) -> "DevicePlan":
+        """Copy the work tables into `buf` (an int32 device tensor of >= device_bytes()
+        bytes) on `stream`, staged through pinned host memory so that the host does
+        not wait for the stream's earlier work."""
+        import torch
+        n = self.device_bytes() // 4
+        dp = self.bind(buf)
+        host = torch.empty(n, dtype=torch.int32, pin_memory=True)
+        _check(_lib.fcp_plan_device_image(self._ptr, C.c_void_p(host.data_ptr()), n * 4),
+               "fcp_plan_device_image")
+        if stream is None:
+            s = torch.cuda.current_stream()
+        elif isinstance(stream, int):
+            s = torch.cuda.ExternalStream(stream)
+        else:
+            s = stream
+        with torch.cuda.stream(s):
+            buf.view(torch.int32)[:n].copy_(host, non_blocking=True)
+        return dp
 
 
 class DevicePlan:

@@ -179,6 +179,27 @@ int64_t fcp_plan_device_bytes(const fcp_plan_t* plan);
 int fcp_plan_upload(const fcp_plan_t* plan, void* dev_buf, int64_t bytes, void* stream,
                     fcp_dev_plan* out);
 
+/*
+ * fcp_plan_device_image -- copy the plan's work tables, exactly the bytes
+ * fcp_plan_upload would send (fcp_plan_device_bytes of them), into host
+ * memory dst[bytes]. The image holds offsets only, so it may be copied to any
+ * 16-byte-aligned device buffer by the caller, e.g. from pinned memory with an
+ * asynchronous copy that does not wait for the stream (a copy from pageable
+ * memory, as fcp_plan_upload makes, can block the host until the stream has
+ * drained). No CUDA call. Errors: FCP_ERR_INVALID_ARG for a null argument,
+ * FCP_ERR_CAPACITY if bytes is too small.
+ */
+int fcp_plan_device_image(const fcp_plan_t* plan, void* dst, int64_t bytes);
+
+/*
+ * fcp_plan_bind -- fill `out` for a device buffer dev_buf[bytes] that holds
+ * (or will hold, before any device call reads it) the plan's image, copied by
+ * the caller. No CUDA call. Errors: FCP_ERR_INVALID_ARG for a null argument or
+ * a dev_buf that is not 16-byte aligned, FCP_ERR_CAPACITY if bytes is too
+ * small.
+ */
+int fcp_plan_bind(const fcp_plan_t* plan, const void* dev_buf, int64_t bytes, fcp_dev_plan* out);
+
 /* ------------------------------------------------------------------------ */
 /* Device operations                                                         */
 /* ------------------------------------------------------------------------ */

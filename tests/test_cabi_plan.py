@@ -162,3 +162,31 @@ def test_work_tables_size(lib):
     p = lib.Plan(D, 4, "perdoc")
     nbytes = p.device_bytes()
     assert nbytes > 0 and nbytes % 256 == 0
+
+
+def test_plan_image_and_bind(lib):
+    """The device image (what an upload sends) and the handle bound to a device
+    address need no CUDA call; the handle's tables lie inside the image."""
+    import ctypes
+    D = synth.doc_lengths(2)
+    p = lib.Plan(D, 4, "perdoc")
+    nbytes = p.device_bytes()
+    img = p.device_image()
+    assert img.nbytes == nbytes and np.array_equal(img, p.device_image())
+    dp = lib.DevPlan()
+    fake = ctypes.c_void_p(1 << 20)                     # never dereferenced: bind makes no CUDA call
+    assert lib.raw_call("fcp_plan_bind", p._ptr, fake, nbytes, ctypes.byref(dp)) == lib.OK
+    assert dp.bytes == nbytes and dp.n_shards == 4 and dp.T == sum(D)
+    assert dp.total_remote_rows == sum(p.shard(j)["remote_rows"] for j in range(4))
+    used = [(dp.tables[t], dp.counts[t]) for t in range(16) if dp.counts[t] > 0]
+    assert used and all(0 <= off < nbytes // 4 for off, _ in used)
+    offs = sorted(off for off, _ in used)
+    assert len(set(offs)) == len(offs)                  # distinct tables
+    assert lib.raw_call("fcp_plan_bind", p._ptr, ctypes.c_void_p((1 << 20) + 4), nbytes,
+                        ctypes.byref(dp)) == lib.ERR_INVALID_ARG   # not 16-byte aligned
+    assert lib.raw_call("fcp_plan_bind", p._ptr, fake, nbytes - 4, ctypes.byref(dp)) == lib.ERR_CAPACITY
+    assert lib.raw_call("fcp_plan_bind", None, fake, nbytes, ctypes.byref(dp)) == lib.ERR_INVALID_ARG
+    small = np.empty(nbytes // 4 - 1, dtype=np.int32)
+    assert lib.raw_call("fcp_plan_device_image", p._ptr, small.ctypes.data_as(ctypes.c_void_p),
+                        small.nbytes) == lib.ERR_CAPACITY
+    assert lib.raw_call("fcp_plan_device_image", p._ptr, None, nbytes) == lib.ERR_INVALID_ARG
