@@ -15,6 +15,8 @@ Readings taken for the Q K^T variant of the forward:
     exact too.
   * Rounding is to the nearest e4m3 value, ties to the even code, and values
     beyond 448 saturate to +-448 ("satfinite").
+  * The scale is held as an fp32 number, so 2^k is kept to fp32's normal
+    range, -126 <= k <= 127 (only an amax below 2^-119 reaches the bound).
 """
 from __future__ import annotations
 
@@ -74,7 +76,8 @@ def pow2_scale_exponent(amax: float) -> int:
         return 0
     m, e = math.frexp(amax)          # amax = m * 2^e, m in [0.5, 1)
     m, e = 2.0 * m, e - 1            # amax = m * 2^e, m in [1, 2)
-    return (8 if m <= 1.75 else 7) - e
+    k = (8 if m <= 1.75 else 7) - e
+    return max(-126, min(127, k))    # 2^k is an fp32 normal number
 
 
 def quantize_tensor(x):

@@ -146,6 +146,8 @@ def test_device_calls_validate_before_launch(lib):
     assert lib.raw_call("fcp_merge", None, None, 17, 10, 4, 64, None, None, None) == lib.ERR_UNSUPPORTED
     assert lib.raw_call("fcp_merge", None, None, 32, 10, 4, 128, None, None, None) == lib.ERR_INVALID_ARG
     assert lib.raw_call("fcp_merge", None, None, 2, 1 << 28, 4, 128, None, None, None) == lib.ERR_UNSUPPORTED
+    assert lib.raw_call("fcp_merge", None, None, 2, 0, 4, 128, None, None, None) == lib.OK   # no rows: nothing to do
+    assert lib.raw_call("fcp_merge", None, None, 2, -1, 4, 128, None, None, None) == lib.ERR_INVALID_ARG
     assert lib.raw_call("fcp_get_device_status", None, None) == lib.ERR_INVALID_ARG
     dm2 = lib.dims(64, 4, 2, 128)
     assert lib.raw_call("fcp_attn_fwd_ring", None, None, None, None, -1, -1, dm2, 0,

@@ -43,6 +43,19 @@ def test_quant_e4m3_bit_exact(cuda, seed, mag):
     assert np.array_equal(codes, ref_codes)
 
 
+@pytest.mark.parametrize("amax_exp", [-119, -120, -126, -130])
+def test_quant_e4m3_tiny_amax_keeps_scale_finite(cuda, amax_exp):
+    """amax at or below 2^-119: the scale stops at 2^127 on both sides."""
+    g = torch.Generator().manual_seed(-amax_exp)
+    x = (torch.rand(4096, generator=g) * 2 - 1) * 2.0 ** amax_exp
+    x[7] = 2.0 ** amax_exp
+    x = x.to(torch.bfloat16)
+    codes, scale = _quant_gpu(x.cuda())
+    ref_codes, k = F.quantize_tensor(x.to(torch.float64).numpy())
+    assert scale == 2.0 ** k and k == 127
+    assert np.array_equal(codes, ref_codes)
+
+
 def _case(D, hq, hkv, d, cp, pol, seed=0):
     from context_document_masked_gb300.session import CPAttention
     T = sum(D)

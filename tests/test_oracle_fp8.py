@@ -49,6 +49,18 @@ def test_power_of_two_scale(amax):
     assert F.pow2_scale_exponent(0.0) == 0
 
 
+def test_scale_exponent_stays_in_fp32_normal_range():
+    """The scale 2^k is an fp32 number: for amax below 2^-119 the largest k
+    with amax * 2^k <= 448 would exceed 127, so k stops at 127."""
+    assert F.pow2_scale_exponent(2.0 ** -119) == 127          # (1.0 <= 1.75) -> 8 + 119
+    assert F.pow2_scale_exponent(1.9 * 2.0 ** -120) == 127    # (1.9 > 1.75) -> 7 + 120
+    assert F.pow2_scale_exponent(2.0 ** -126) == 127
+    assert F.pow2_scale_exponent(2.0 ** -133) == 127          # a bf16 subnormal
+    assert F.pow2_scale_exponent(2.0 ** -118) == 126
+    codes, k = F.quantize_tensor(np.full(4, 2.0 ** -126))
+    assert k == 127 and list(codes) == [0x40] * 4              # 2^-126 * 2^127 = 2.0 = code 0x40
+
+
 def test_dequantized_tensor_error_within_half_ulp():
     rng = np.random.default_rng(0)
     x = rng.standard_normal(10000) * 3
