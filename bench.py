@@ -464,7 +464,6 @@ def _bench_e2e(args, D, w, seed, torch, CPAttention, fcp):
     in_ready, comp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
     fwd_done = [ev(), ev()]
     pairs = sum(L * (L + 1) // 2 for L in D)
-    state = {"i": 0, "copied": False}
 
     sessions = [None, None]
 
