@@ -100,7 +100,7 @@ int32_t host_at(const Plan* p, int tb, int64_t i) { return p->dev[p->tab_off[tb]
 int check_dims(const fcp_dims& d, const Plan* p) {
   if (d.T <= 0 || d.hq <= 0 || d.hkv <= 0) return FCP_ERR_INVALID_ARG;
   if (d.d != 64 && d.d != 128) return FCP_ERR_UNSUPPORTED;
-  if (d.hq % d.hkv != 0 || (d.hq / d.hkv) % 2 != 0) return FCP_ERR_UNSUPPORTED;
+  if (d.hq % d.hkv != 0) return FCP_ERR_UNSUPPORTED;
   if (p && d.T != p->T) return FCP_ERR_INVALID_ARG;
   return FCP_OK;
 }

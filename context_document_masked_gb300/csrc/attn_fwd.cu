@@ -12,8 +12,10 @@
 //
 // Work unit: one 128-row query tile of one piece (a shard's query range inside
 // one document) for TWO query heads of the same GQA group, which read the
-// same K/V tiles. Key tiles are 128 keys of one key segment (a run of keys
-// held by the shard or received from others), so only tiles that contain
+// same K/V tiles (a group of odd size, MHA included, pairs its last head with
+// a repeat of itself whose results are not stored; that form of the kernel is
+// a separate instantiation). Key tiles are 128 keys of one key segment (a run
+// of keys held by the shard or received from others), so only tiles that contain
 // useful (q, k) pairs are visited; tiles on the diagonal or at a segment end
 // are masked element by element.
 //
@@ -121,11 +123,17 @@ __device__ __forceinline__ int count_key_tiles(const int32_t* segs, int seg_begi
 }
 
 struct WorkItem {
-  int q_start, q_rows, seg_begin, seg_count, h0, g;
+  int q_start, q_rows, seg_begin, seg_count, h0, h1, g;
 };
 
+// Head pairs per query tile: each GQA group's heads two at a time; an odd
+// group's last pair holds one head (its second slot repeats the first and
+// stores nothing).
+__host__ __device__ __forceinline__ int head_pairs(int hq, int hkv) { return hkv * ((hq / hkv + 1) / 2); }
+
+template <bool ODD>
 __device__ __forceinline__ WorkItem decode(const FwdParams& p, int w) {
-  const int hp_count = p.hq / 2;
+  const int hp_count = ODD ? head_pairs(p.hq, p.hkv) : p.hq / 2;
   const int item = __ldg(p.order + w / hp_count);
   const int hp = w % hp_count;
   const int* t = p.tiles + 4 * item;
@@ -135,12 +143,20 @@ __device__ __forceinline__ WorkItem decode(const FwdParams& p, int w) {
   it.q_rows = __ldg(t + 2);
   it.seg_begin = __ldg(p.pieces + 8 * piece + 5);
   it.seg_count = __ldg(p.pieces + 8 * piece + 6);
-  it.h0 = 2 * hp;
-  it.g = it.h0 / (p.hq / p.hkv);
+  if constexpr (ODD) {
+    const int G = p.hq / p.hkv, per_group = (G + 1) / 2;
+    it.g = hp / per_group;
+    it.h0 = it.g * G + 2 * (hp % per_group);
+    it.h1 = it.h0 + 1 < (it.g + 1) * G ? it.h0 + 1 : it.h0;
+  } else {
+    it.h0 = 2 * hp;
+    it.h1 = it.h0 + 1;
+    it.g = it.h0 / (p.hq / p.hkv);
+  }
   return it;
 }
 
-template <int D, bool QK8>
+template <int D, bool QK8, bool ODD>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kb,
@@ -194,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
   const WaitCtl wc{&abort_sh, p.err, p.wait_ns};
-  const int n_work = p.n_items * (p.hq / 2);
+  const int n_work = p.n_items * (ODD ? head_pairs(p.hq, p.hkv) : p.hq / 2);
 
   uint8_t* sQ = smem + C::kQOff;
   uint8_t* sKV = smem + C::kKVOff;
@@ -209,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t k = 0;
       for (int w = blockIdx.x; ok; w = next_work(p.work_counter)) {
         if (!(ok = ring.put<true>(k++, w, wc)) || w >= n_work) break;
-        const WorkItem it = decode(p, w);
+        const WorkItem it = decode<ODD>(p, w);
         const int q_last = it.q_start + it.q_rows - 1;
         const int nt = count_key_tiles(p.segs, it.seg_begin, it.seg_count, q_last, p.kv_lo, p.kv_hi, p.seg_filter);
         if (nt == 0) continue;
@@ -217,12 +233,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (QK8) {  // e4m3 rows of D bytes: one box per head
           mbar_arrive_expect_tx(&bar_q_full, 2 * 128 * D);
           for (int h = 0; h < 2; ++h)
-            tma_load_3d(sQ + h * C::kTileBytes, &tm_q, &bar_q_full, 0, it.h0 + h, it.q_start);
+            tma_load_3d(sQ + h * C::kTileBytes, &tm_q, &bar_q_full, 0, h ? it.h1 : it.h0, it.q_start);
         } else {
           mbar_arrive_expect_tx(&bar_q_full, 2 * C::kTileBytes);
           for (int h = 0; h < 2; ++h)
             for (int pn = 0; pn < C::kPanels; ++pn)
-              tma_load_3d(sQ + h * C::kTileBytes + pn * 16384, &tm_q, &bar_q_full, pn * 64, it.h0 + h,
+              tma_load_3d(sQ + h * C::kTileBytes + pn * 16384, &tm_q, &bar_q_full, pn * 64, h ? it.h1 : it.h0,
                           it.q_start);
         }
         ++q_iter;
@@ -294,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = ring.get<true>(k, w, wc))) break;
         ring.release(k);
         if (w >= n_work) break;
-        const WorkItem it = decode(p, w);
+        const WorkItem it = decode<ODD>(p, w);
         const int q_last = it.q_start + it.q_rows - 1;
         const int nt = count_key_tiles(p.segs, it.seg_begin, it.seg_count, q_last, p.kv_lo, p.kv_hi, p.seg_filter);
         if (nt == 0) continue;
@@ -366,12 +382,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) ring.release(k);
       if (w >= n_work) break;
-      const WorkItem it = decode(p, w);
+      const WorkItem it = decode<ODD>(p, w);
       const int q_last = it.q_start + it.q_rows - 1;
       const int nt = count_key_tiles(p.segs, it.seg_begin, it.seg_count, q_last, p.kv_lo, p.kv_hi, p.seg_filter);
       const int q = it.q_start + r;
-      const bool row_valid = r < it.q_rows;
-      const int head = it.h0 + i;
+      bool row_valid = r < it.q_rows;
+      int head = it.h0 + i;
       float m_run = -INFINITY, l = 0.f;
       if (nt > 0) {
         Walker wk;
@@ -464,7 +480,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++o_cnt;
         tc_fence_after();
       }
-      // Epilogue: O / l and LSE for this row.
+      // Epilogue: O / l and LSE for this row. The second slot of an odd
+      // group's last pair repeats the first head: it runs but stores nothing.
+      if constexpr (ODD) {
+        head = i ? it.h1 : it.h0;
+        row_valid = row_valid && (i == 0 || it.h1 != it.h0);
+      }
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const size_t obase = ((size_t)q * p.hq + head) * D;
 #pragma unroll 1
@@ -530,31 +551,36 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-template <int D, bool QK8>
+template <int D, bool QK8, bool ODD>
 static int launch_fwd_impl(const FwdLaunch& a, cudaStream_t st) {
   using C = FwdCfg<D>;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(attn_fwd_kernel<D, QK8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(attn_fwd_kernel<D, QK8, ODD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemAlloc) != cudaSuccess)
       return FCP_ERR_CUDA;
     attr_set[dev] = true;
   }
-  const int n_work = a.p.n_items * (a.p.hq / 2);
+  const int n_work = a.p.n_items * head_pairs(a.p.hq, a.p.hkv);
   if (n_work == 0) return FCP_OK;
   const int grid = n_work < a.num_sms ? n_work : a.num_sms;
-  attn_fwd_kernel<D, QK8><<<grid, kThreads, C::kSmemAlloc, st>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_kb, a.tm_vb,
+  attn_fwd_kernel<D, QK8, ODD><<<grid, kThreads, C::kSmemAlloc, st>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_kb, a.tm_vb,
                                                                 a.p);
   return cudaGetLastError() == cudaSuccess ? FCP_OK : FCP_ERR_CUDA;
 }
 
-int launch_attn_fwd(const FwdLaunch& a, cudaStream_t st) {
-  if (a.qk8) return a.d == 128 ? launch_fwd_impl<128, true>(a, st) : FCP_ERR_UNSUPPORTED;
-  if (a.d == 128) return launch_fwd_impl<128, false>(a, st);
-  if (a.d == 64) return launch_fwd_impl<64, false>(a, st);
+template <bool ODD>
+static int launch_fwd_any(const FwdLaunch& a, cudaStream_t st) {
+  if (a.qk8) return a.d == 128 ? launch_fwd_impl<128, true, ODD>(a, st) : FCP_ERR_UNSUPPORTED;
+  if (a.d == 128) return launch_fwd_impl<128, false, ODD>(a, st);
+  if (a.d == 64) return launch_fwd_impl<64, false, ODD>(a, st);
   return FCP_ERR_UNSUPPORTED;
+}
+
+int launch_attn_fwd(const FwdLaunch& a, cudaStream_t st) {
+  return (a.p.hq / a.p.hkv) % 2 ? launch_fwd_any<true>(a, st) : launch_fwd_any<false>(a, st);
 }
 
 }  // namespace fcp

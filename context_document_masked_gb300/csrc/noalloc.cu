@@ -101,7 +101,7 @@ extern "C" int fcp_attn_fwd_noalloc(const void* q, const void* k, const void* v,
   const fcp::Plan* p = plan->host;
   if (dims.T <= 0 || dims.hq <= 0 || dims.hkv <= 0 || dims.T != p->T) return FCP_ERR_INVALID_ARG;
   if (dims.d != 64 && dims.d != 128) return FCP_ERR_UNSUPPORTED;
-  if (dims.hq % dims.hkv != 0 || (dims.hq / dims.hkv) % 2 != 0) return FCP_ERR_UNSUPPORTED;
+  if (dims.hq % dims.hkv != 0) return FCP_ERR_UNSUPPORTED;
   if (!q || !k || !v || !out || !lse) return FCP_ERR_INVALID_ARG;
   if (out_dtype != FCP_OUT_BF16 && out_dtype != FCP_OUT_F32) return FCP_ERR_INVALID_ARG;
   if (kv_lo < 0 || kv_hi > dims.T || kv_lo > kv_hi) return FCP_ERR_INVALID_ARG;

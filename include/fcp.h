@@ -21,7 +21,7 @@
  *   - Token-major varlen layout: Q and O are [T][Hq][d], K and V [T][Hkv][d],
  *     all contiguous, row-major; LSE is [Hq][T] fp32, natural log.
  *   - Query head h reads KV head h / (Hq/Hkv) (contiguous GQA groups).
- *   - Supported: d in {64, 128}, Hq % Hkv == 0, Hq/Hkv even, T < 2^31.
+ *   - Supported: d in {64, 128}, Hq % Hkv == 0 (any group size, MHA included), T < 2^31.
  *   - All device pointers must be 16-byte aligned.
  */
 #ifndef FCP_H

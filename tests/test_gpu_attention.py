@@ -26,6 +26,8 @@ SMALL = [
     ("tiles_edges", [1, 127, 128, 129, 255, 256, 1, 1, 600, 2], 4, 2, 128, 3, "perdoc"),
     ("long_doc_gqa4", [3000, 40, 1, 55], 8, 2, 128, 2, "perdoc"),
     ("single_doc", [1536], 4, 2, 128, 2, "llama3"),
+    ("mha_d128_perdoc", synth.random_doc_lengths(1024, seed=11), 4, 4, 128, 4, "perdoc"),
+    ("gqa3_d64_hybrid", synth.random_doc_lengths(1536, seed=12), 6, 2, 64, 3, "hybrid"),
 ]
 
 
@@ -208,7 +210,7 @@ def test_merge_kernel_against_oracle(cuda, B, d):
     assert np.max(np.abs(lg[fin] - l_ref[fin])) <= TOL_LSE
 
 
-BWD = [SMALL[0], SMALL[1], SMALL[3], SMALL[5], SMALL[6]]
+BWD = [SMALL[0], SMALL[1], SMALL[3], SMALL[5], SMALL[6], SMALL[8], SMALL[9]]
 
 
 @pytest.mark.parametrize("case", BWD, ids=[c[0] for c in BWD])

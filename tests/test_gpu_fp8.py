@@ -68,6 +68,7 @@ CASES = [
     ("ragged_d128_hybrid", synth.random_doc_lengths(2048, seed=9), 8, 2, 128, 4, "hybrid"),
     ("tiles_edges", [1, 127, 128, 129, 255, 256, 1, 1, 600, 2], 4, 2, 128, 3, "perdoc"),
     ("long_doc_gqa4", [3000, 40, 1, 55], 8, 2, 128, 2, "perdoc"),
+    ("mha_d128", synth.random_doc_lengths(1024, seed=14), 4, 4, 128, 2, "perdoc"),
 ]
 
 

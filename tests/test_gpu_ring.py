@@ -25,6 +25,7 @@ CASES = [
     ("cfg1_llama3", synth.doc_lengths(1), 4, 2, 64, 2, "llama3"),
     ("ragged_d128_perdoc", synth.random_doc_lengths(1024, seed=7), 4, 2, 128, 4, "perdoc"),
     ("ragged_d128_hybrid", synth.random_doc_lengths(2048, seed=9), 8, 2, 128, 4, "hybrid"),
+    ("gqa3_d128_perdoc", synth.random_doc_lengths(1536, seed=13), 6, 2, 128, 3, "perdoc"),
     ("tiles_edges_perdoc", [1, 127, 128, 129, 255, 256, 1, 1, 600, 2], 4, 2, 128, 3, "perdoc"),
     ("long_doc_wholedoc", [3000, 40, 1, 55, 900], 8, 2, 128, 4, "wholedoc"),
 ]
