@@ -7,10 +7,12 @@
 // ReduceScatter of the KV gradients; on one GPU that reduction is the
 // scatter-add of every key tile's dK/dV into the keys' global rows.
 //
-// Work unit: one key tile (<= 128 keys of one key segment of one piece) for
-// one KV head. The CTA loops over the query heads of that GQA group and the
-// piece's query tiles that can see the keys, so dK and dV accumulate in TMEM
-// over the whole group and reach global memory once per unit.
+// Work unit: one key tile (<= 128 keys of one key segment) for one KV head.
+// The CTA loops over the query heads of that GQA group and the query tiles
+// that can see the keys -- those of the piece, and of the shard's earlier
+// piece of the same document when the tile lies before that piece's end -- so
+// dK and dV accumulate in TMEM over the whole group and reach global memory
+// once per unit.
 //
 // Per step (one query head, one 128-row query tile), with keys as rows:
 //   S^T = K Q^T, dP^T = V dO^T                (TMEM)
@@ -72,24 +74,45 @@ struct BwdCfg {
 };
 
 struct BwdItem {
-  int piece_start, piece_end, key0, n, src, src_row, qt_first, n_qt, g;
+  int key0, n, src, src_row, qa0, qa_end, na, qb0, qb_end, nb, nq, g;
 };
 
 __device__ __forceinline__ BwdItem decode(const BwdParams& p, int w) {
   const int item = __ldg(p.order + w / p.hkv);
-  const int* t = p.tiles + 8 * item;
-  const int piece = __ldg(t + 0);
+  const int* t = p.tiles + kBwdTileInts * item;
   BwdItem it;
-  it.piece_start = __ldg(p.pieces + 8 * piece + 2);
-  it.piece_end = __ldg(p.pieces + 8 * piece + 3);
-  it.key0 = __ldg(t + 2);
-  it.n = __ldg(t + 3);
-  it.src = __ldg(t + 4);
-  it.src_row = __ldg(t + 5) - (it.src ? p.kbuf_shift : 0);
-  it.qt_first = __ldg(t + 6);
-  it.n_qt = __ldg(t + 7);
+  it.key0 = __ldg(t + 0);
+  it.n = __ldg(t + 1);
+  it.src = __ldg(t + 2);
+  it.src_row = __ldg(t + 3) - (it.src ? p.kbuf_shift : 0);
+  it.qa0 = __ldg(t + 4);
+  it.qa_end = __ldg(t + 5);
+  it.na = __ldg(t + 6);
+  it.qb0 = __ldg(t + 7);
+  it.qb_end = __ldg(t + 8);
+  it.nb = __ldg(t + 9);
+  it.nq = it.na + it.nb;
   it.g = w % p.hkv;
   return it;
+}
+
+// Query tile of step j of a unit: head index within the group j / nq, then
+// the first range's tiles and the second range's.
+struct StepRows {
+  int h, q0, q_end;
+};
+__device__ __forceinline__ StepRows step_rows(const BwdItem& it, int G, int j) {
+  StepRows r;
+  const int jh = j / it.nq, jj = j - jh * it.nq;
+  r.h = it.g * G + jh;
+  if (jj < it.na) {
+    r.q0 = it.qa0 + jj * 128;
+    r.q_end = it.qa_end;
+  } else {
+    r.q0 = it.qb0 + (jj - it.na) * 128;
+    r.q_end = it.qb_end;
+  }
+  return r;
 }
 
 // TMA bulk reduce-add of a shared-memory tile into global memory.
@@ -230,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       ++kv_items;
-      const int nsteps = G * it.n_qt;
+      const int nsteps = G * it.nq;
       // L2 prefetches: the next unit's K/V tiles now, each step's Q/dO tiles
       // two steps ahead, so the shared-memory loads above hit in L2.
       if (lane == 0 && w_next < n_work) {
@@ -241,15 +264,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       for (int j = 0; j < nsteps; ++j) {
-        const int h = it.g * G + j / it.n_qt;
-        const int q0 = it.piece_start + (it.qt_first + j % it.n_qt) * 128;
-        const int q_rows = min(128, it.piece_end - q0);
+        const StepRows sr = step_rows(it, G, j);
+        const int h = sr.h, q0 = sr.q0;
+        const int q_rows = min(128, sr.q_end - q0);
         if (lane == 0 && j + 2 < nsteps) {
-          const int h2 = it.g * G + (j + 2) / it.n_qt;
-          const int q2 = it.piece_start + (it.qt_first + (j + 2) % it.n_qt) * 128;
+          const StepRows s2 = step_rows(it, G, j + 2);
           for (int pn = 0; pn < C::kPanels; ++pn) {
-            tma_prefetch_3d(&tm_q, pn * 64, h2, q2);
-            tma_prefetch_3d(&tm_do, pn * 64, h2, q2);
+            tma_prefetch_3d(&tm_q, pn * 64, s2.h, s2.q0);
+            tma_prefetch_3d(&tm_do, pn * 64, s2.h, s2.q0);
           }
         }
         // Q tile and the rows' LSE / D into Q stage s.
@@ -333,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ring.release(k);
         if (w >= n_work) break;
         const BwdItem it = decode(p, w);
-        const int nsteps = G * it.n_qt;
+        const int nsteps = G * it.nq;
         if (!(ok = mbar_wait(&bar_kv_conv, kv_items & 1, wc))) break;
         tc_fence_after();
         // Prologue of the unit: S_0 and dP_0.
@@ -442,12 +464,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) ring.release(k);
       if (w >= n_work) break;
       const BwdItem it = decode(p, w);
-      const int nsteps = G * it.n_qt;
+      const int nsteps = G * it.nq;
       const bool key_valid = kr < it.n;
       const int key = it.key0 + kr;
       for (int j = 0; j < nsteps; ++j, ++gstep) {
         const uint32_t c = qc + j, s = c & 1;
-        const int q0 = it.piece_start + (it.qt_first + j % it.n_qt) * 128;
+        const int q0 = step_rows(it, G, j).q0;
         const int lim = key - q0 - 64 * half;  // local columns below lim cannot see this key
         // Whole tile below the diagonal with 128 keys: no element needs a mask
         // (query rows past the piece end have LSE = +inf, hence P = 0).
@@ -599,10 +621,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) ring.release(k);
       if (w >= n_work) break;
       const BwdItem it = decode(p, w);
-      const int nsteps = G * it.n_qt;
+      const int nsteps = G * it.nq;
       for (int j = 0; j < nsteps; ++j, ++gstep) {
-        const int h = it.g * G + j / it.n_qt;
-        const int q0 = it.piece_start + (it.qt_first + j % it.n_qt) * 128;
+        const StepRows sr = step_rows(it, G, j);
+        const int h = sr.h, q0 = sr.q0;
         ok = drain_group_all(mbar_wait(&bar_dq_full, gstep & 1, wc));
         if (!ok) break;
         tc_fence_after();

@@ -9,6 +9,9 @@
 
 namespace fcp {
 
+// Ints per backward unit in the plan's TB_BTILES table.
+constexpr int kBwdTileInts = 12;
+
 struct FwdParams {
   const int32_t* pieces;   // plan piece table
   const int32_t* segs;     // key segments
@@ -39,7 +42,7 @@ struct FwdLaunch {
 
 struct BwdParams {
   const int32_t* pieces;
-  const int32_t* tiles;    // backward key tiles (piece, seg, key0, n, src, src_row, qt_first, n_qt)
+  const int32_t* tiles;    // backward units, kBwdTileInts ints each (plan.h, TB_BTILES)
   const int32_t* order;
   int32_t n_items;
   int32_t kbuf_shift;

@@ -35,7 +35,9 @@ enum Table {
   TB_FTILES,       // 4 ints: piece, q_start, q_rows, cost   (grouped by shard)
   TB_FORDER,       // all-shards longest-first order of TB_FTILES
   TB_FSHARD,       // N+1 offsets into TB_FTILES
-  TB_BTILES,       // 8 ints: piece, seg, key_start, key_rows, src, src_row, q_first, cost
+  TB_BTILES,       // kBwdTileInts ints: key_start, key_rows, src, src_row, then two query
+                   // ranges (first tile start, piece end, tile count; the first may be
+                   // empty), piece, seg
   TB_BORDER,
   TB_BSHARD,
   TB_COPY,         // 4 ints: src_row, dst_row, nrows, shard (grouped by shard)

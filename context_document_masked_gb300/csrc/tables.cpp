@@ -7,7 +7,12 @@
 //     and runs received from other shards (read from the compacted
 //     kbuf/vbuf, in the order of the shard's kv_remote list);
 //   - forward query tiles of <= 128 rows, each inside one piece;
-//   - backward key tiles of <= 128 keys, each inside one segment;
+//   - backward units: key tiles of <= 128 keys, each inside one segment,
+//     with the query tiles that see them. Where a shard holds two pieces of
+//     one document, every key tile of the earlier piece is also a key tile of
+//     the later one (both walks cut [doc start, earlier end) at the same
+//     points), so that tile is one unit whose steps run over both pieces'
+//     query tiles: dK/dV of the tile leave the kernel once, not twice;
 //   - gather runs (<= kCopyRows rows) and preprocess row chunks.
 // Tiles are listed piece by piece (pieces ordered by their longest tile) and,
 // inside a piece, longest first (by the number of tile pairs they cover): the
@@ -17,6 +22,7 @@
 #include <array>
 #include <numeric>
 
+#include "kernels.h"
 #include "plan.h"
 
 namespace fcp {
@@ -70,11 +76,12 @@ void Plan::build_work_tables() {
   std::vector<int32_t> fshard(N + 1, 0), bshard(N + 1, 0), cshard(N + 1, 0), rshard(N + 1, 0);
   std::vector<int64_t> fcost, bcost;
   std::vector<int32_t> fpiece, bpiece;
+  struct PieceInfo { int32_t id, doc, start, end, seg_begin, seg_count; };
   int32_t piece_id = 0;
   for (int32_t j = 0; j < N; ++j) {
     const Shard& sh = shards[j];
     fshard[j] = (int32_t)(ftiles.size() / 4);
-    bshard[j] = (int32_t)(btiles.size() / 8);
+    bshard[j] = (int32_t)(btiles.size() / kBwdTileInts);
     cshard[j] = (int32_t)(copy.size() / 4);
     rshard[j] = (int32_t)(rows.size() / 2);
     // Position of each remote range inside this shard's kbuf.
@@ -89,6 +96,7 @@ void Plan::build_work_tables() {
       }
       acc += rr.end - rr.start;
     }
+    std::vector<PieceInfo> pinfo;
     for (const Piece& p : sh.pieces) {
       const int32_t ds = off[p.doc];
       const int32_t seg_begin = (int32_t)segs.size();
@@ -132,30 +140,53 @@ void Plan::build_work_tables() {
         shards[j].fwd_qtiles += 1;
         shards[j].fwd_masked += count_masked_tiles(segs, seg_begin, seg_count, q0, q0 + qr - 1);
       }
-      // Backward key tiles: every tile of every segment; the queries that see
-      // it are the piece's rows at or after the tile start.
-      for (int32_t s = seg_begin; s < seg_begin + seg_count; ++s) {
-        const Seg& g = segs[s];
-        for (int32_t k0 = 0; k0 < g.len; k0 += kTileN) {
-          int32_t kr = std::min(kTileN, g.len - k0);
-          int32_t key = g.key_start + k0;
-          int32_t qfirst = std::max(key, p.start);
-          int32_t qt_first = (qfirst - p.start) / kTileM;
-          int32_t n_qt = (p.end - p.start + kTileM - 1) / kTileM - qt_first;
-          btiles.insert(btiles.end(), {piece_id, s, key, kr, g.src, g.src_row + k0, qt_first, n_qt});
-          bcost.push_back(n_qt);
-          bpiece.push_back(piece_id);
-          shards[j].bwd_tiles += n_qt;
-          shards[j].bwd_ktiles += 1;
-        }
-      }
+      pinfo.push_back(PieceInfo{piece_id, p.doc, p.start, p.end, seg_begin, seg_count});
       for (int32_t a = p.start; a < p.end; a += kRowChunk)
         rows.insert(rows.end(), {a, std::min(kRowChunk, p.end - a)});
       ++piece_id;
     }
+    // Backward units: every key tile of every segment of a piece; the queries
+    // that see it are the piece's rows at or after the tile start. A document
+    // with exactly two pieces in this shard gives one unit per key tile of the
+    // later piece, the earlier piece's query tiles attached to the tiles that
+    // lie before its end.
+    auto q_tiles = [](const PieceInfo& pc, int32_t key, int32_t* q0, int32_t* n) {
+      const int32_t qt_first = (std::max(key, pc.start) - pc.start) / kTileM;
+      *q0 = pc.start + qt_first * kTileM;
+      *n = (pc.end - pc.start + kTileM - 1) / kTileM - qt_first;
+    };
+    for (size_t i = 0; i < pinfo.size(); ++i) {
+      const PieceInfo& pc = pinfo[i];
+      int n_same = 0, partner = -1;
+      for (size_t o = 0; o < pinfo.size(); ++o)
+        if (pinfo[o].doc == pc.doc) {
+          ++n_same;
+          if (o != i) partner = (int)o;
+        }
+      if (n_same != 2) partner = -1;
+      if (partner >= 0 && pinfo[partner].start > pc.start) continue;  // emitted with the later piece
+      for (int32_t s = pc.seg_begin; s < pc.seg_begin + pc.seg_count; ++s) {
+        const Seg& g = segs[s];
+        for (int32_t k0 = 0; k0 < g.len; k0 += kTileN) {
+          const int32_t kr = std::min(kTileN, g.len - k0);
+          const int32_t key = g.key_start + k0;
+          int32_t qa0 = 0, qa_end = 0, na = 0, qb0, nb;
+          if (partner >= 0 && key < pinfo[partner].end) {
+            q_tiles(pinfo[partner], key, &qa0, &na);
+            qa_end = pinfo[partner].end;
+          }
+          q_tiles(pc, key, &qb0, &nb);
+          btiles.insert(btiles.end(), {key, kr, g.src, g.src_row + k0, qa0, qa_end, na, qb0, pc.end, nb, pc.id, s});
+          bcost.push_back(na + nb);
+          bpiece.push_back(pc.id);
+          shards[j].bwd_tiles += na + nb;
+          shards[j].bwd_ktiles += 1;
+        }
+      }
+    }
   }
   fshard[N] = (int32_t)(ftiles.size() / 4);
-  bshard[N] = (int32_t)(btiles.size() / 8);
+  bshard[N] = (int32_t)(btiles.size() / kBwdTileInts);
   cshard[N] = (int32_t)(copy.size() / 4);
   rshard[N] = (int32_t)(rows.size() / 2);
   // Piece-major, longest-first orders. A piece's rank is the position of its
@@ -195,7 +226,7 @@ void Plan::build_work_tables() {
     piece.swap(pout);
   };
   sort_group(ftiles, 4, fcost, fpiece, frank, fshard, N);
-  sort_group(btiles, 8, bcost, bpiece, brank, bshard, N);
+  sort_group(btiles, kBwdTileInts, bcost, bpiece, brank, bshard, N);
   std::vector<int32_t> forder(fcost.size()), border(bcost.size());
   std::iota(forder.begin(), forder.end(), 0);
   std::iota(border.begin(), border.end(), 0);
@@ -251,7 +282,7 @@ void Plan::build_work_tables() {
   append(dev, tab_off, tab_cnt, TB_FTILES, ftiles, (int32_t)(ftiles.size() / 4));
   append(dev, tab_off, tab_cnt, TB_FORDER, forder, (int32_t)forder.size());
   append(dev, tab_off, tab_cnt, TB_FSHARD, fshard, N + 1);
-  append(dev, tab_off, tab_cnt, TB_BTILES, btiles, (int32_t)(btiles.size() / 8));
+  append(dev, tab_off, tab_cnt, TB_BTILES, btiles, (int32_t)(btiles.size() / kBwdTileInts));
   append(dev, tab_off, tab_cnt, TB_BORDER, border, (int32_t)border.size());
   append(dev, tab_off, tab_cnt, TB_BSHARD, bshard, N + 1);
   append(dev, tab_off, tab_cnt, TB_COPY, copy, (int32_t)(copy.size() / 4));

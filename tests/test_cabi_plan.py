@@ -71,8 +71,12 @@ def _tile_counts(shard, cu, tile=128):
     pieces and received ranges: a piece's keys [doc start, piece end) form
     maximal runs held by the shard or received; the forward walks them per
     query tile up to its last query, the backward takes every key tile of
-    every run with the piece's query tiles from the first that sees it."""
+    every run with the piece's query tiles from the first that sees it. A
+    backward unit is one distinct key tile: where a document has exactly two
+    pieces in the shard, the earlier piece's key tiles must all be key tiles
+    of the later piece too (checked here), and each is one unit."""
     fwd = qt = masked = bwd = kt = 0
+    tiles_of = {}
     for pc in shard.pieces:
         ds = int(cu[pc.doc])
         runs, t = [], ds
@@ -93,11 +97,19 @@ def _tile_counts(shard, cu, tile=128):
                     fwd += 1
                     masked += int(k + tile - 1 > q0 or end - k < tile)
         n_qt_all = -(-(pc.end - pc.start) // tile)
+        tiles_of[(pc.doc, pc.start)] = set()
         for ks, ln in runs:
             for k0 in range(0, ln, tile):
                 key = ks + k0
                 bwd += n_qt_all - (max(key, pc.start) - pc.start) // tile
-                kt += 1
+                tiles_of[(pc.doc, pc.start)].add((key, min(tile, ln - k0)))
+    for pc in shard.pieces:
+        same = sorted(o.start for o in shard.pieces if o.doc == pc.doc)
+        mine = tiles_of[(pc.doc, pc.start)]
+        if len(same) == 2 and pc.start == same[0]:
+            assert mine <= tiles_of[(pc.doc, same[1])]
+        else:
+            kt += len(mine)
     return fwd, qt, masked, bwd, kt
 
 
