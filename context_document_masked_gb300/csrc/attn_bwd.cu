@@ -234,7 +234,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
       ++k;
       if (!ok || w >= n_work) break;
-      // The next unit is claimed now, so its tiles can be prefetched into L2.
+      // The next unit is claimed now (measured a little ahead of claiming it
+      // after this unit's loads).
       int w_next = 0;
       if (lane == 0) w_next = next_work(p.work_counter);
       w_next = __shfl_sync(0xffffffffu, w_next, 0);
@@ -254,26 +255,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ++kv_items;
       const int nsteps = G * it.nq;
-      // L2 prefetches: the next unit's K/V tiles now, each step's Q/dO tiles
-      // two steps ahead, so the shared-memory loads above hit in L2.
-      if (lane == 0 && w_next < n_work) {
-        const BwdItem nx = decode(p, w_next);
-        for (int pn = 0; pn < C::kPanels; ++pn) {
-          tma_prefetch_3d(nx.src ? &tm_kb : &tm_k, pn * 64, nx.g, nx.src_row);
-          tma_prefetch_3d(nx.src ? &tm_vb : &tm_v, pn * 64, nx.g, nx.src_row);
-        }
-      }
+      // No L2 prefetches: issued through the tensor-memory accelerator, which
+      // also carries this CTA's loads and dQ reduce-adds, they cost more in its
+      // queue than they saved.
       for (int j = 0; j < nsteps; ++j) {
         const StepRows sr = step_rows(it, G, j);
         const int h = sr.h, q0 = sr.q0;
         const int q_rows = min(128, sr.q_end - q0);
-        if (lane == 0 && j + 2 < nsteps) {
-          const StepRows s2 = step_rows(it, G, j + 2);
-          for (int pn = 0; pn < C::kPanels; ++pn) {
-            tma_prefetch_3d(&tm_q, pn * 64, s2.h, s2.q0);
-            tma_prefetch_3d(&tm_do, pn * 64, s2.h, s2.q0);
-          }
-        }
         // Q tile and the rows' LSE / D into Q stage s.
         const int s = qc & 1;
         if (qc >= 2) {
