@@ -47,8 +47,8 @@ BWD_TRAFFIC = {
                 ("context_document_masked_gb300/csrc/kernels.h", "struct BwdParams", "int launch_attn_fwd"),
                 ("context_document_masked_gb300/csrc/api.cu", "int fcp_attn_bwd(", "int fcp_get_device_status("),
                 ("context_document_masked_gb300/csrc/tables.cpp", None, None)],
-    "sha256": "1ffbabd41a416a1978a8b63027eec1fa2fe1355dd0cfc17c2b43b46fa0e7b569",
-    "bytes": (2.771157 + 1.421134 + 1.087443 + 1.044086) * 1e9,
+    "sha256": "99b942df565637e2f31b17863c1acb473229ad0b4b6842ad8a60bd1692c82b0e",
+    "bytes": (2.523194 + 1.397763 + 1.087234 + 1.043908) * 1e9,
 }
 
 
@@ -514,9 +514,15 @@ def _bench_e2e(args, D, w, seed, torch, CPAttention, fcp):
 
     run(3)
     n = max(4, args.steps // 2)
-    t0 = time.perf_counter()
-    run(n)
-    dt = (time.perf_counter() - t0) / n
+    # Three timed runs of n steps each; the median run is reported (one host
+    # stall in a run -- allocation, page-in, another process -- otherwise
+    # moves the whole figure).
+    runs = []
+    for _ in range(3):
+        t0 = time.perf_counter()
+        run(n)
+        runs.append((time.perf_counter() - t0) / n)
+    dt = sorted(runs)[1]
     h2d_bytes = sum(x.numel() * x.element_size() for x in (q, k, v, do))
     d2h_bytes = sum(x.numel() * x.element_size() for x in h_out[0])
     return {"value": round((14.0 * d * hq * pairs) / dt / 1e12, 2), "unit": UNIT, "ms_per_step": round(dt * 1e3, 3),
@@ -524,7 +530,8 @@ def _bench_e2e(args, D, w, seed, torch, CPAttention, fcp):
             "includes": "per step: H2D of Q,K,V,dO; plan build + upload + buffer allocation; gather; fwd; "
                         "bwd; D2H of O (fp32, as soon as the forward ends), dQ, dK, dV -- copies of "
                         "neighbouring steps overlap this step's kernels on separate streams; wall time "
-                        "over the whole run"}
+                        "of the median of three runs of n steps",
+            "runs_ms_per_step": [round(x * 1e3, 3) for x in runs]}
 
 
 def _cpu_baseline(seconds: float):
