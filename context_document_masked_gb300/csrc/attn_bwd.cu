@@ -553,15 +553,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t src_col = lane_base + (half == 0 ? C::kColDV : C::kColDK);
       const float mul = half == 0 ? 1.f : p.scale;
       const CUtensorMap* tm_out = half == 0 ? &tm_dv : &tm_dk;
-#pragma unroll 1
-      for (int cc = 0; cc < D / 32 && ok; ++cc, ++stg) {
-        float v[32];
-        tmem_ld32(src_col + cc * 32, v);
-        tmem_ld_wait();
+      // Two chunks in registers: the TMEM read of chunk cc + 2 is issued once
+      // chunk cc is staged and waited for two chunks later, so its latency
+      // (a TMEM read waits behind the MMAs' own TMEM traffic) overlaps the
+      // reduce-adds of the chunks between.
+      constexpr int kChunks = D / 32;
+      float vv[2][32];
+      tmem_ld32(src_col, vv[0]);
+      tmem_ld32(src_col + 32, vv[1]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int cc = 0; cc < kChunks; ++cc, ++stg) {
+        if (!ok) break;
+        float* v = vv[cc & 1];
         if (stg > 0) {  // the previous chunk's reduce has read the staging tile
           ok = mbar_wait(&bar_stg_free[half], (stg - 1) & 1, wc);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         }
+        if (cc >= 2) tmem_ld_wait();  // this chunk was read after chunk cc - 2 was staged
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4) {
           const float a0 = key_valid ? v[4 * q4] * mul : 0.f, a1 = key_valid ? v[4 * q4 + 1] * mul : 0.f;
@@ -571,6 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();
         mbar_arrive(&bar_stg_full[half]);
+        if (cc + 2 < kChunks) tmem_ld32(src_col + (cc + 2) * 32, vv[cc & 1]);
         if (kr == 0) {
           ok = mbar_wait(&bar_stg_full[half], stg & 1, wc);
           if (ok) {
@@ -582,6 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ok = __all_sync(0xffffffffu, ok);  // the issuing lane's outcome, warp-wide
       }
+      tmem_ld_wait();  // no TMEM read left in flight, also when the loop gave up early
       // The last chunk's tile is read before dS of the next unit lands there.
       if (ok) ok = mbar_wait(&bar_stg_free[half], (stg - 1) & 1, wc);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
