@@ -47,8 +47,8 @@ BWD_TRAFFIC = {
                 ("context_document_masked_gb300/csrc/kernels.h", "struct BwdParams", "int launch_attn_fwd"),
                 ("context_document_masked_gb300/csrc/api.cu", "int fcp_attn_bwd(", "int fcp_get_device_status("),
                 ("context_document_masked_gb300/csrc/tables.cpp", None, None)],
-    "sha256": "99b942df565637e2f31b17863c1acb473229ad0b4b6842ad8a60bd1692c82b0e",
-    "bytes": (2.523194 + 1.397763 + 1.087234 + 1.043908) * 1e9,
+    "sha256": "e66543d175af5c034103b8ae745777c80f6d90009236d0c50b3e6abba18307a8",
+    "bytes": (2.545627 + 1.412386 + 1.087044 + 1.043522) * 1e9,
 }
 
 
