@@ -217,9 +217,15 @@ typedef struct {
  * of Q, K and the received K rows with their scales (fcp_attn_fwd_qk8), the
  * backward's row statistics D_i = <dO_i, O_i> ([Hq][T] fp32), fp16 copies of
  * Q and dO ([T][Hq][d] each, the backward's tensor-core operands) and of V and
- * the plan's received V rows (the forward's P*V operands). Calls that share a
- * workspace must be ordered on the GPU (one stream, or synchronised): two at
- * once would race on these contents. */
+ * the plan's received V rows (the forward's P*V operands). The caller
+ * zero-fills a new workspace once before its first call: the error word must
+ * start at zero (fcp_get_device_status clears it after reporting an error),
+ * and a one-shard backward reads the fp16 Q and dO rows of whole 128-row
+ * tiles, rows of other shards included, which must hold finite values (their
+ * probabilities are zero, but 0 * NaN is not); each call writes the rows of
+ * its own shard before reading them. Calls that share a workspace must be
+ * ordered on the GPU (one stream, or synchronised): two at once would race on
+ * these contents. */
 int64_t fcp_workspace_bytes(fcp_dims dims, const fcp_plan_t* plan);
 
 /*
