@@ -204,3 +204,83 @@ def test_plan_image_and_bind(lib):
     assert lib.raw_call("fcp_plan_device_image", p._ptr, small.ctypes.data_as(ctypes.c_void_p),
                         small.nbytes) == lib.ERR_CAPACITY
     assert lib.raw_call("fcp_plan_device_image", p._ptr, None, nbytes) == lib.ERR_INVALID_ARG
+
+
+TB_BTILES, TB_BSHARD, BWD_INTS = 5, 7, 12
+
+
+def _bwd_units(got):
+    """The plan's backward units as the kernel reads them: the device image
+    decoded through the offsets fcp_plan_bind reports (a host buffer serves:
+    binding computes offsets only)."""
+    import ctypes as C
+    img = got.device_image()
+    from context_document_masked_gb300 import fcp as F
+    h = F.DevPlan()
+    buf = np.zeros(img.size + 4, dtype=np.int32)
+    base = buf.ctypes.data
+    base += (-base) % 16
+    assert F._lib.fcp_plan_bind(got.handle, C.c_void_p(base), img.nbytes, C.byref(h)) == 0
+    off, n = h.tables[TB_BTILES], h.counts[TB_BTILES]
+    units = img[off:off + n * BWD_INTS].reshape(n, BWD_INTS)
+    so = h.tables[TB_BSHARD]
+    shard_of = np.zeros(n, dtype=np.int64)
+    bounds = img[so:so + h.n_shards + 1]
+    for j in range(h.n_shards):
+        shard_of[bounds[j]:bounds[j + 1]] = j
+    return units, shard_of
+
+
+@pytest.mark.parametrize("name,D,N,pol,R", CASES[:20] + CASES[-40:], ids=[c[0] for c in CASES[:20] + CASES[-40:]])
+def test_backward_units_cover_each_shards_tiles(lib, name, D, N, pol, R):
+    """Every backward unit names one key tile and the query tiles that see it.
+    Per shard, the units cover each distinct key tile of its pieces once, and a
+    unit's query tiles are exactly those of the shard's pieces of that
+    document holding a query at or after the tile's first key (re-derived from
+    the oracle plan); the key rows are read from K/V (own keys) or from the
+    shard's slice of the gathered buffer (received keys)."""
+    ref = P.make_plan(D, N, pol, R)
+    got = lib.Plan(D, N, pol, R)
+    cu = synth.cu_from_lengths(D)
+    units, shard_of = _bwd_units(got)
+    tile = 128
+    for j in range(N):
+        sh = ref.shards[j]
+        kbase = got.shard(j)["kbuf_base"]
+        # Received rows of this shard, in kbuf order.
+        rpos, acc = {}, 0
+        for (doc, a, b) in sh.kv_remote:
+            rpos[(doc, a, b)] = acc
+            acc += b - a
+        want = {}
+        for pc in sh.pieces:
+            ds = int(cu[pc.doc])
+            t = ds
+            while t < pc.end:
+                own = [o for o in sh.pieces if o.doc == pc.doc and o.start <= t < o.end]
+                rem = [r for r in sh.kv_remote if r[0] == pc.doc and r[1] <= t < r[2]]
+                e = min(own[0].end if own else rem[0][2], pc.end)
+                for k0 in range(t, e, tile):
+                    kr = min(tile, e - k0)
+                    src_row = k0 if own else kbase + rpos[tuple(rem[0])] + (k0 - rem[0][1])
+                    qts = set()
+                    for o in sh.pieces:
+                        if o.doc == pc.doc and o.end > k0:
+                            first = (max(k0, o.start) - o.start) // tile
+                            qts |= {o.start + tile * i for i in range(first, -(-(o.end - o.start) // tile))}
+                    want[(pc.doc, k0, kr)] = (0 if own else 1, src_row, qts)
+                t = e
+        got_units = {}
+        for u in units[shard_of == j]:
+            key, kr, src, srow, qa0, qa_end, na, qb0, qb_end, nb = (int(x) for x in u[:10])
+            doc = int(np.searchsorted(cu, key, side="right") - 1)
+            assert (doc, key, kr) not in got_units, "key tile listed twice"
+            qts = {qa0 + tile * i for i in range(na)} | {qb0 + tile * i for i in range(nb)}
+            assert len(qts) == na + nb
+            for q0, n_t, end in ((qa0, na, qa_end), (qb0, nb, qb_end)):
+                if n_t:  # the range's last tile holds the piece's last query
+                    assert q0 + tile * (n_t - 1) < end <= q0 + tile * n_t
+            got_units[(doc, key, kr)] = (src, srow, qts)
+        assert got_units.keys() == want.keys()
+        for key_tile, val in want.items():
+            assert got_units[key_tile] == val, key_tile
