@@ -284,3 +284,134 @@ def test_backward_units_cover_each_shards_tiles(lib, name, D, N, pol, R):
         assert got_units.keys() == want.keys()
         for key_tile, val in want.items():
             assert got_units[key_tile] == val, key_tile
+
+
+TB = dict(PIECES=0, SEGS=1, FTILES=2, FSHARD=4, COPY=8, CSHARD=9, ROWS=10, RSHARD=11, KBASE=13,
+          RPIECES=14, RSEGS=15)
+
+
+def _tables(got):
+    """Every work table of the device image, as int32 rows, through the
+    offsets and counts fcp_plan_bind reports for a host buffer."""
+    import ctypes as C
+    from context_document_masked_gb300 import fcp as F
+    img = got.device_image()
+    h = F.DevPlan()
+    buf = np.zeros(img.size + 4, dtype=np.int32)
+    base = buf.ctypes.data
+    base += (-base) % 16
+    assert F._lib.fcp_plan_bind(got.handle, C.c_void_p(base), img.nbytes, C.byref(h)) == 0
+    width = dict(PIECES=8, SEGS=4, FTILES=4, FSHARD=1, COPY=4, CSHARD=1, ROWS=2, RSHARD=1, KBASE=1,
+                 RPIECES=8, RSEGS=4)
+    out = {}
+    for name, t in TB.items():
+        off, n = h.tables[t], h.counts[t]
+        out[name] = img[off:off + n * width[name]].reshape(n, width[name])
+    return out
+
+
+def _walk(sh, pc, cu):
+    """A piece's needed keys [doc start, piece end) as (key_start, len, own,
+    remote range) runs, cut where the shard's own pieces and received ranges
+    meet."""
+    runs, t = [], int(cu[pc.doc])
+    while t < pc.end:
+        own = [o for o in sh.pieces if o.doc == pc.doc and o.start <= t < o.end]
+        rem = [r for r in sh.kv_remote if r[0] == pc.doc and r[1] <= t < r[2]]
+        e = min(own[0].end if own else rem[0][2], pc.end)
+        runs.append((t, e - t, bool(own), None if own else tuple(rem[0])))
+        t = e
+    return runs
+
+
+@pytest.mark.parametrize("name,D,N,pol,R", CASES[:20] + CASES[-40:], ids=[c[0] for c in CASES[:20] + CASES[-40:]])
+def test_forward_tables_match_oracle_walk(lib, name, D, N, pol, R):
+    """The forward's work tables against the oracle plan: pieces in shard
+    order; each piece's key segments cover [doc start, piece end) with own keys
+    read at their global rows and received keys at their row of the shard's
+    slice of the gathered buffer; query tiles of <= 128 rows cut each piece,
+    each with the count of key tiles it visits; gather runs of <= 32 rows copy
+    each received range into consecutive buffer rows; preprocess row chunks
+    cover each piece."""
+    ref = P.make_plan(D, N, pol, R)
+    got = lib.Plan(D, N, pol, R)
+    cu = synth.cu_from_lengths(D)
+    tb = _tables(got)
+    kbase = [int(x) for x in tb["KBASE"][:, 0]]
+    assert kbase[N] == sum(got.shard(j)["remote_rows"] for j in range(N))
+    pieces = tb["PIECES"]
+    pi = 0
+    for j in range(N):
+        sh = ref.shards[j]
+        rpos, acc = {}, kbase[j]
+        for r in sh.kv_remote:
+            rpos[tuple(r)] = acc
+            acc += r[2] - r[1]
+        assert acc == kbase[j + 1]
+        for pc in sh.pieces:
+            row = [int(x) for x in pieces[pi]]
+            assert row[:5] == [j, pc.doc, pc.start, pc.end, int(cu[pc.doc])]
+            segs = tb["SEGS"][row[5]:row[5] + row[6]]
+            want = [(0, k, k, n) if own else (1, rpos[rem] + k - rem[1], k, n) for k, n, own, rem in _walk(sh, pc, cu)]
+            assert [tuple(int(x) for x in s_) for s_ in segs] == want
+            tiles = [t for t in tb["FTILES"] if t[0] == pi]
+            assert sorted((int(t[1]), int(t[2])) for t in tiles) == [(q, min(128, pc.end - q))
+                                                                     for q in range(pc.start, pc.end, 128)]
+            assert all(tiles[a][3] >= tiles[a + 1][3] for a in range(len(tiles) - 1))  # longest first
+            for t in tiles:
+                q_last = int(t[1] + t[2] - 1)
+                visits = sum(-(-min(n, q_last - k + 1) // 128) for _, _, k, n in want if k <= q_last)
+                assert int(t[3]) == visits
+            pi += 1
+        # A shard's tiles are grouped piece by piece inside its slice of the table.
+        ft = tb["FTILES"][tb["FSHARD"][j, 0]:tb["FSHARD"][j + 1, 0]]
+        order = [int(t[0]) for t in ft]
+        assert sorted(set(order)) == list(range(pi - len(sh.pieces), pi))
+        for x in set(order):
+            at = [a for a, v in enumerate(order) if v == x]
+            assert at == list(range(at[0], at[-1] + 1))
+        copies = tb["COPY"][tb["CSHARD"][j, 0]:tb["CSHARD"][j + 1, 0]]
+        want_c = []
+        for r in sh.kv_remote:
+            for a in range(r[1], r[2], 32):
+                want_c.append((a, rpos[tuple(r)] + a - r[1], min(32, r[2] - a), j))
+        assert [tuple(int(x) for x in c) for c in copies] == want_c
+        rows = tb["ROWS"][tb["RSHARD"][j, 0]:tb["RSHARD"][j + 1, 0]]
+        assert [tuple(int(x) for x in r) for r in rows] == [(a, min(128, pc.end - a)) for pc in sh.pieces
+                                                           for a in range(pc.start, pc.end, 128)]
+    assert pi == len(pieces)
+
+
+@pytest.mark.parametrize("name,D,N,pol,R", CASES[:20] + CASES[-40:], ids=[c[0] for c in CASES[:20] + CASES[-40:]])
+def test_ring_tables_list_owner_runs_by_distance(lib, name, D, N, pol, R):
+    """Ring order ("LLM Context Parallel in Production", "Ring Attention"): a
+    piece's needed keys cut into runs by the shard that owns them (adjacent
+    runs of one owner joined), listed by ring distance (shard - owner) mod N,
+    own keys first, each read at its global rows."""
+    ref = P.make_plan(D, N, pol, R)
+    got = lib.Plan(D, N, pol, R)
+    cu = synth.cu_from_lengths(D)
+    tb = _tables(got)
+    owner = np.full(int(cu[-1]), -1)
+    for j, sh in enumerate(ref.shards):
+        for pc in sh.pieces:
+            owner[pc.start:pc.end] = j
+    assert (owner >= 0).all()
+    rp = tb["RPIECES"]
+    i = 0
+    for j, sh in enumerate(ref.shards):
+        for pc in sh.pieces:
+            row = [int(x) for x in rp[i]]
+            assert row[:5] == [j, pc.doc, pc.start, pc.end, int(cu[pc.doc])]
+            runs = []
+            for t in range(int(cu[pc.doc]), pc.end):
+                dist = (j - int(owner[t])) % N
+                if runs and runs[-1][0] == dist and runs[-1][1] + runs[-1][2] == t:
+                    runs[-1][2] += 1
+                else:
+                    runs.append([dist, t, 1])
+            runs.sort(key=lambda r: r[0])  # stable: key order inside one distance
+            segs = tb["RSEGS"][row[5]:row[5] + row[6]]
+            assert [tuple(int(x) for x in s_) for s_ in segs] == [(d_, k, k, n) for d_, k, n in runs]
+            i += 1
+    assert i == len(rp)
