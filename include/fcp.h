@@ -95,7 +95,9 @@ typedef struct {
   int64_t fwd_qtiles;          /* forward query tiles                              */
   int64_t fwd_masked;          /* forward tiles needing a per-element mask         */
   int64_t bwd_tiles;           /* backward key-tile x query-tile pairs             */
-  int64_t bwd_ktiles;          /* backward key tiles (per KV head)                 */
+  int64_t bwd_ktiles;          /* backward work units (per KV head): the shard's   */
+                               /* distinct key tiles (a key tile shared by two     */
+                               /* pieces of one document is one unit)              */
 } fcp_shard_view;
 
 typedef struct {
