@@ -119,6 +119,10 @@ int64_t remote_rows_of(const Plan* p, int32_t shard) {
 
 }  // namespace
 
+namespace fcp {
+int64_t wait_limit_ns() { return g_wait_ns; }
+}  // namespace fcp
+
 extern "C" {
 
 const char* fcp_strerror(int s) {
@@ -261,6 +265,9 @@ struct WsLayout {
 // scales 2^kq and 2^kk.
 constexpr int64_t kQkAmaxOff = 128;
 constexpr int64_t kQkScaleOff = 136;
+// Diagnostic counter of the forward: online-softmax rescales of O after a
+// query tile's first key tile (one count per warp and event).
+constexpr int64_t kRescaleCountOff = 192;
 
 static int64_t ws_align(int64_t x) { return (x + 255) / 256 * 256; }
 
@@ -401,6 +408,7 @@ static int attn_fwd_impl(const void* q, const void* k, const void* v, const void
   fp.err = static_cast<int*>(ws);
   fp.work_counter = counter;
   fp.qk_scale = qk8 ? reinterpret_cast<const float*>(wsb + kQkScaleOff) : nullptr;
+  fp.rescale_count = reinterpret_cast<int*>(wsb + kRescaleCountOff);
   fp.wait_ns = g_wait_ns;
   a.d = dims.d;
   a.num_sms = num_sms();
@@ -431,6 +439,13 @@ int fcp_quant_e4m3(const void* x, int64_t n, void* out, float* scale_out, void* 
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(scratch, 0, sizeof(unsigned), cs) != cudaSuccess) return FCP_ERR_CUDA;
   return fcp::launch_quant_e4m3(x, out, n, static_cast<unsigned*>(scratch), scale_out, num_sms(), cs);
+}
+
+int fcp_round_bf16(const float* x, int64_t n, void* out, void* stream) {
+  if (n < 0 || n % 8 != 0) return FCP_ERR_INVALID_ARG;
+  if (n == 0) return FCP_OK;
+  if (!x || !out || !aligned16(x) || !aligned16(out)) return FCP_ERR_INVALID_ARG;
+  return fcp::launch_round_bf16(x, out, n, num_sms(), static_cast<cudaStream_t>(stream));
 }
 
 int fcp_attn_fwd_ring(const void* q, const void* k, const void* v, const fcp_dev_plan* plan,
@@ -548,5 +563,17 @@ int fcp_get_device_status(void* ws, void* stream) {
 }
 
 void fcp_debug_set_wait_limit(int64_t ns) { g_wait_ns = ns == 0 ? 2000000000LL : ns; }
+
+int fcp_debug_rescale_events(void* ws, void* stream, int64_t* count) {
+  if (!ws || !count) return FCP_ERR_INVALID_ARG;
+  int word = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* counter = static_cast<char*>(ws) + kRescaleCountOff;
+  if (cudaMemcpyAsync(&word, counter, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return FCP_ERR_CUDA;
+  if (cudaMemsetAsync(counter, 0, sizeof(int), s) != cudaSuccess) return FCP_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FCP_ERR_CUDA;
+  *count = word;
+  return FCP_OK;
+}
 
 }  // extern "C"

@@ -459,6 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float rowsum = ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
           // P_i(t-1) V has completed (see above), so O_i can be rescaled now.
           if (t > 0 && __any_sync(0xffffffffu, rescale)) {
+            if (lane == 0 && p.rescale_count) atomicAdd(p.rescale_count, 1);
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
               float v[32];

@@ -263,6 +263,19 @@ __global__ void __launch_bounds__(kCvtThreads)
   if (ovf) atomicOr(err, 4);
 }
 
+// ------------------------------------------------------- fp32 -> bf16
+// The final-output form of an fp32 O: each element rounded to the nearest
+// bf16 (ties to even). Eight elements per thread: two 16-byte loads, one
+// 16-byte store.
+__global__ void __launch_bounds__(kCvtThreads)
+    round_bf16_kernel(const float4* __restrict__ src, uint4* __restrict__ dst, int64_t n) {
+  for (int64_t i = (int64_t)blockIdx.x * kCvtThreads + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * kCvtThreads) {
+    const float4 a = __ldg(src + 2 * i), b = __ldg(src + 2 * i + 1);
+    dst[i] = make_uint4(pack2(a.x, a.y), pack2(a.z, a.w), pack2(b.x, b.y), pack2(b.z, b.w));
+  }
+}
+
 // ------------------------------------------------------- e4m3 quantisation
 // Per-tensor power-of-two scale 2^k, the largest with max|x| * 2^k <= 448
 // (the largest finite e4m3 value), so scaling and dequantising are exact;
@@ -353,6 +366,16 @@ int launch_convert_f16(const void* src, void* dst, int64_t n_elems, int* err, in
   if (grid < 1) grid = 1;
   convert_kernel<<<(int)grid, kCvtThreads, 0, st>>>(static_cast<const uint4*>(src),
                                                     static_cast<uint4*>(dst), n, err, zero_word);
+  return cudaGetLastError() == cudaSuccess ? FCP_OK : FCP_ERR_CUDA;
+}
+
+int launch_round_bf16(const float* src, void* dst, int64_t n_elems, int num_sms, cudaStream_t st) {
+  const int64_t n = n_elems / 8;
+  if (n == 0) return FCP_OK;
+  int64_t grid = (n + kCvtThreads - 1) / kCvtThreads;
+  if (grid > (int64_t)num_sms * 16) grid = (int64_t)num_sms * 16;
+  round_bf16_kernel<<<(int)grid, kCvtThreads, 0, st>>>(reinterpret_cast<const float4*>(src),
+                                                       static_cast<uint4*>(dst), n);
   return cudaGetLastError() == cudaSuccess ? FCP_OK : FCP_ERR_CUDA;
 }
 

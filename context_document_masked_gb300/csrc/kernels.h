@@ -29,6 +29,7 @@ struct FwdParams {
   int* err;
   int* work_counter;       // zero at launch (set by the preceding kernel of the call)
   const float* qk_scale;   // e4m3 Q K^T variant: the scales 2^kq, 2^kk of Q and K (else unused)
+  int* rescale_count;      // if not null: +1 per warp each time O is rescaled after a later key tile
   int64_t wait_ns;
 };
 
@@ -71,6 +72,9 @@ struct BwdLaunch {
 int launch_attn_fwd(const FwdLaunch& a, cudaStream_t st);
 int launch_attn_bwd(const BwdLaunch& a, cudaStream_t st);
 
+// Limit of every bounded device wait (fcp_debug_set_wait_limit), in ns.
+int64_t wait_limit_ns();
+
 // Row statistics D_i = <dO_i, O_i> for the rows of the given row chunks, dQ
 // rows set to zero, and fp16 copies of Q and dO for the backward's MMAs.
 // *zero_word (if not null) is set to 0: the work counter of the kernel that
@@ -85,6 +89,10 @@ int launch_bwd_preprocess(const void* out, bool out_f32, const void* dout, const
 // (if not null) is set to 0, as above.
 int launch_convert_f16(const void* src, void* dst, int64_t n_elems, int* err, int* zero_word,
                        int num_sms, cudaStream_t st);
+
+// bf16 copy (round to nearest even) of an fp32 array of n_elems (a multiple
+// of 8) elements.
+int launch_round_bf16(const float* src, void* dst, int64_t n_elems, int num_sms, cudaStream_t st);
 
 // e4m3 copy of a bf16 array of n_elems (a multiple of 8) elements, scaled by
 // the power of two 2^k, the largest with max|x| * 2^k <= 448 (exact to undo).

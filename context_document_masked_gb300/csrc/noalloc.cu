@@ -175,7 +175,8 @@ extern "C" int fcp_attn_fwd_noalloc(const void* q, const void* k, const void* v,
   fp.lse = lse;
   fp.err = err;
   fp.work_counter = counter;
-  fp.wait_ns = 2000000000LL;
+  fp.rescale_count = nullptr;
+  fp.wait_ns = fcp::wait_limit_ns();
   a.d = dims.d;
   a.num_sms = num_sms();
   return fcp::launch_attn_fwd(a, cs);

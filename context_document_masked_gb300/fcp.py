@@ -24,6 +24,7 @@ EXPORTED = (
     "fcp_workspace_bytes", "fcp_gather_kv", "fcp_attn_fwd", "fcp_merge", "fcp_attn_bwd",
     "fcp_get_device_status", "fcp_debug_set_wait_limit", "fcp_attn_fwd_noalloc", "fcp_attn_fwd_ring",
     "fcp_attn_fwd_qk8", "fcp_quant_e4m3", "fcp_plan_device_image", "fcp_plan_bind",
+    "fcp_debug_rescale_events", "fcp_round_bf16",
 )
 
 
@@ -103,6 +104,8 @@ def _load():
         "fcp_attn_fwd_noalloc": (C.c_int, [vp, vp, vp, vp, vp, C.POINTER(DevPlan), i32, i32, i32, Dims,
                                            i32, vp, vp, vp]),
         "fcp_debug_set_wait_limit": (None, [i64]),
+        "fcp_debug_rescale_events": (C.c_int, [vp, vp, C.POINTER(i64)]),
+        "fcp_round_bf16": (C.c_int, [vp, i64, vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -325,6 +328,12 @@ def attn_fwd_noalloc(q, k, v, kbuf, vbuf, dplan: DevicePlan, shard: int, out, ls
            "fcp_attn_fwd_noalloc")
 
 
+def round_bf16(x, out, stream=None):
+    """fcp_round_bf16: out (bf16, same element count) = x (fp32) rounded to nearest even."""
+    assert x.numel() == out.numel()
+    _check(_lib.fcp_round_bf16(_ptr(x), x.numel(), _ptr(out), _stream(stream)), "fcp_round_bf16")
+
+
 def merge(o_parts, lse_parts, out, lse_out, stream=None):
     B, rows, hq, d = o_parts.shape
     _check(_lib.fcp_merge(_ptr(o_parts), _ptr(lse_parts), B, rows, hq, d, _ptr(out), _ptr(lse_out),
@@ -349,6 +358,13 @@ def device_status(ws, stream=None) -> int:
 
 def debug_set_wait_limit(ns: int):
     _lib.fcp_debug_set_wait_limit(ns)
+
+
+def debug_rescale_events(ws, stream=None) -> int:
+    """Rescales of O after a later key tile since the last read (then cleared)."""
+    n = C.c_int64()
+    _check(_lib.fcp_debug_rescale_events(_ptr(ws), _stream(stream), C.byref(n)), "fcp_debug_rescale_events")
+    return int(n.value)
 
 
 def raw_call(name: str, *args):

@@ -291,6 +291,18 @@ int fcp_attn_fwd_qk8(const void* q, const void* k, const void* v, const void* kb
                      void* out, float* lse, void* ws, int64_t ws_bytes, void* stream);
 
 /*
+ * fcp_round_bf16 -- bf16 copy of an fp32 array, each element rounded to the
+ * nearest bf16 value (ties to even). The final output of the forward is bf16
+ * ([FlashCP] trains in bf16); a caller that keeps the fp32 output of
+ * fcp_attn_fwd for the backward's D_i = <dO_i, O_i> rounds it once with this
+ * call for its own use. Equals fcp_attn_fwd's FCP_OUT_BF16 output bit for bit.
+ *   x    fp32 [n], out bf16 [n]; n a multiple of 8; both 16-byte aligned.
+ * Errors: FCP_ERR_INVALID_ARG (n not a multiple of 8, null or misaligned
+ * pointers when n > 0).
+ */
+int fcp_round_bf16(const float* x, int64_t n, void* out, void* stream);
+
+/*
  * fcp_attn_fwd_ring -- the same forward in ring order, without a gathered
  * key buffer ([CPGuide] "Ring Attention": at step s of the ring, shard j
  * holds the KV block of shard (j - s) mod N and merges its partial result by
@@ -375,7 +387,10 @@ int fcp_attn_bwd(const void* q, const void* k, const void* v, const void* kbuf,
  *   it (the error word is cleared at the start of each call): calls whose work
  *   can overlap on the GPU -- on different streams without ordering -- race and
  *   must not be issued. Device-side timeouts of this variant are recorded in
- *   the shared array only; use fcp_attn_fwd with a workspace to read them.
+ *   the shared array only, and so is an input of V (or of the received V rows)
+ *   beyond the fp16 range |x| > 65504, which fcp_attn_fwd reports as
+ *   FCP_ERR_UNSUPPORTED: this variant gives inf/NaN in O and LSE for such
+ *   input without an error. Use fcp_attn_fwd with a workspace to detect both.
  */
 int fcp_attn_fwd_noalloc(const void* q, const void* k, const void* v, const void* kbuf,
                          const void* vbuf, const fcp_dev_plan* plan, int32_t shard,
@@ -397,6 +412,20 @@ int fcp_get_device_status(void* ws, void* stream);
  * sets the error word, drains its copies and MMAs, frees TMEM and returns)
  * without a hang. */
 void fcp_debug_set_wait_limit(int64_t ns);
+
+/*
+ * fcp_debug_rescale_events -- diagnostic read of the forward kernels' rescale
+ * counter in the workspace header (synchronizes the stream, then clears it).
+ * The online softmax ([CPGuide] "Core Principle: Split Q, Circulate KV")
+ * keeps a running row maximum m; the kernels rescale the accumulated O only
+ * when a later key tile raises m by more than 2^8 (log2 units), so that the
+ * unnormalised probabilities stay <= 2^8. *count receives the number of such
+ * rescales (one count per 32-row warp and event) made by fcp_attn_fwd,
+ * fcp_attn_fwd_qk8 and fcp_attn_fwd_ring on this workspace since the last
+ * read; a new, zero-filled workspace starts at 0. Errors: FCP_ERR_INVALID_ARG
+ * for a null argument, FCP_ERR_CUDA if the read fails.
+ */
+int fcp_debug_rescale_events(void* ws, void* stream, int64_t* count);
 
 #ifdef __cplusplus
 }

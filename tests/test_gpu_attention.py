@@ -134,6 +134,35 @@ def test_first_token_row_is_exact(cuda):
             assert torch.equal(out[st, h].cpu(), v[st, h // 2])
 
 
+def test_round_bf16_is_the_forward_bf16_output(cuda):
+    """fcp_round_bf16 of the fp32 output equals the forward's own bf16 output,
+    and, on random values with exact ties, subnormals, infinities and values
+    near the bf16 maximum, equals round-to-nearest-even (PyTorch's CPU cast)."""
+    from context_document_masked_gb300 import fcp
+    case = SMALL[3]
+    name, D, hq, hkv, d, cp, pol = case
+    s, cu, q, k, v, qd, kd, vd = _setup(*case)
+    s.gather(kd, vd)
+    out32, _ = s.forward(qd, kd, vd, out_dtype=torch.float32)
+    out16, _ = s.forward(qd, kd, vd)
+    r = torch.empty_like(out16)
+    fcp.round_bf16(out32, r)
+    torch.cuda.synchronize()
+    assert torch.equal(r, out16)
+    g = torch.Generator().manual_seed(5)
+    x = torch.randn(1 << 16, generator=g) * torch.exp2(torch.randint(-140, 128, (1 << 16,), generator=g).float())
+    bits = torch.randint(0, 1 << 16, (4096,), generator=g, dtype=torch.int32)
+    x[:4096] = ((bits << 16) | 0x8000).view(torch.float32)     # exactly halfway between two bf16
+    x[4096:4100] = torch.tensor([float("inf"), -float("inf"), 3.3895e38, -0.0])
+    x = x[torch.isfinite(x) | torch.isinf(x)]
+    x = x[: x.numel() // 8 * 8]
+    y = torch.empty(x.numel(), dtype=torch.bfloat16, device="cuda")
+    fcp.round_bf16(x.cuda(), y)
+    torch.cuda.synchronize()
+    ref = x.to(torch.bfloat16)
+    assert torch.equal(y.cpu().view(torch.int16), ref.view(torch.int16))
+
+
 def test_gather_is_byte_exact(cuda):
     D = synth.doc_lengths(2)[:5]
     T = sum(D) - sum(D) % 8
