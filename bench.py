@@ -674,7 +674,7 @@ def _bench_e2e(args, D, w, seed, torch, fcp):
         torch.cuda.synchronize()
 
     big = T > 200000
-    run(1 if big else 3)
+    run(2 if big else 3)              # both buffer sets warmed (allocator, pinned pages)
     n = args.e2e_steps if big else max(4, args.steps // 2)
     reps = 1 if big else 3
     # Timed runs of n steps each; with several runs the median is reported (one
@@ -768,8 +768,9 @@ def main():
                     help="headline workload (1: 2K d=64, 2: 32K, 3: 128K, 4: 64K short docs, 5: 512K)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=3.0)
-    ap.add_argument("--e2e-steps", type=int, default=2,
-                    help="timed end-to-end steps on workloads above 200K tokens (their copies take ~1 min a step)")
+    ap.add_argument("--e2e-steps", type=int, default=4,
+                    help="timed end-to-end steps on workloads above 200K tokens (one run of them; smaller "
+                         "workloads take the median of three runs of max(4, steps / 2))")
     ap.add_argument("--legs", default="step,merge,ring,configs,shards,e2e,cpu",
                     help="parts to run: step (always), merge, ring, configs (the other workloads), shards "
                          "(per-shard calibration), e2e, cpu; e.g. 'step' for profiling")
