@@ -78,7 +78,8 @@ struct BwdItem {
 };
 
 __device__ __forceinline__ BwdItem decode(const BwdParams& p, int w) {
-  const int item = __ldg(p.order + w / p.hkv);
+  const WorkSlot ws = work_slot(w, p.n_items, p.hkv, p.order_block);
+  const int item = __ldg(p.order + ws.pos);
   const int* t = p.tiles + kBwdTileInts * item;
   BwdItem it;
   it.key0 = __ldg(t + 0);
@@ -92,7 +93,7 @@ __device__ __forceinline__ BwdItem decode(const BwdParams& p, int w) {
   it.qb_end = __ldg(t + 8);
   it.nb = __ldg(t + 9);
   it.nq = it.na + it.nb;
-  it.g = w % p.hkv;
+  it.g = ws.head;
   return it;
 }
 
@@ -699,8 +700,12 @@ static int launch_bwd_impl(const BwdLaunch& a, cudaStream_t st) {
   const int n_work = a.p.n_items * a.p.hkv;
   if (n_work == 0) return FCP_OK;
   const int grid = n_work < a.num_sms ? n_work : a.num_sms;
+  // Blocks of key tiles that fill the grid with one KV head: the CTAs running
+  // together stream the same query rows (Q, dO, dQ) of that head group.
+  BwdParams p = a.p;
+  p.order_block = grid;
   attn_bwd_kernel<D><<<grid, kThreads, C::kSmem, st>>>(a.tm_q, a.tm_do, a.tm_k, a.tm_v, a.tm_kb,
-                                                      a.tm_vb, a.tm_dq, a.tm_dk, a.tm_dv, a.p);
+                                                      a.tm_vb, a.tm_dq, a.tm_dk, a.tm_dv, p);
   return cudaGetLastError() == cudaSuccess ? FCP_OK : FCP_ERR_CUDA;
 }
 

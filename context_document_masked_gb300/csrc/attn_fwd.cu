@@ -134,8 +134,9 @@ __host__ __device__ __forceinline__ int head_pairs(int hq, int hkv) { return hkv
 template <bool ODD>
 __device__ __forceinline__ WorkItem decode(const FwdParams& p, int w) {
   const int hp_count = ODD ? head_pairs(p.hq, p.hkv) : p.hq / 2;
-  const int item = __ldg(p.order + w / hp_count);
-  const int hp = w % hp_count;
+  const WorkSlot ws = work_slot(w, p.n_items, hp_count, p.order_block);
+  const int item = __ldg(p.order + ws.pos);
+  const int hp = ws.head;
   const int* t = p.tiles + 4 * item;
   const int piece = __ldg(t + 0);
   WorkItem it;
@@ -567,8 +568,13 @@ static int launch_fwd_impl(const FwdLaunch& a, cudaStream_t st) {
   const int n_work = a.p.n_items * head_pairs(a.p.hq, a.p.hkv);
   if (n_work == 0) return FCP_OK;
   const int grid = n_work < a.num_sms ? n_work : a.num_sms;
+  // Blocks of query tiles such that one block's head pairs of one KV head
+  // fill the grid: the CTAs running together stream the same K/V rows.
+  FwdParams p = a.p;
+  const int pairs_per_kv = head_pairs(p.hq, p.hkv) / p.hkv;
+  p.order_block = grid / pairs_per_kv > 0 ? grid / pairs_per_kv : 1;
   attn_fwd_kernel<D, QK8, ODD><<<grid, kThreads, C::kSmemAlloc, st>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_kb, a.tm_vb,
-                                                                a.p);
+                                                                p);
   return cudaGetLastError() == cudaSuccess ? FCP_OK : FCP_ERR_CUDA;
 }
 

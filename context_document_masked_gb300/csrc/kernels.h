@@ -30,6 +30,7 @@ struct FwdParams {
   int* work_counter;       // zero at launch (set by the preceding kernel of the call)
   const float* qk_scale;   // e4m3 Q K^T variant: the scales 2^kq, 2^kk of Q and K (else unused)
   int* rescale_count;      // if not null: +1 per warp each time O is rescaled after a later key tile
+  int32_t order_block;     // work decode: items per block (set by the launch, see work_slot)
   int64_t wait_ns;
 };
 
@@ -57,6 +58,7 @@ struct BwdParams {
   float* dv;
   int* err;
   int* work_counter;       // zero at launch (set by the preprocess)
+  int32_t order_block;     // work decode: items per block (set by the launch, see work_slot)
   int64_t wait_ns;
 };
 

@@ -156,6 +156,27 @@ struct WorkRing {
 // Next work index for this CTA after its first (blockIdx.x).
 __device__ __forceinline__ int next_work(int* counter) { return (int)gridDim.x + atomicAdd(counter, 1); }
 
+// Work index w -> (position in the item order, head index). A work list is
+// n_items items (tiles, longest first) x n_heads heads. Items go in blocks of
+// `block`; inside a block the head is the slow index, so the CTAs running at
+// one time work on the same head of neighbouring items and share that head's
+// key/value (or query) rows in L2, while the blocks keep the longest-first
+// order. Requires 0 <= w < n_items * n_heads and block >= 1.
+struct WorkSlot {
+  int pos, head;
+};
+__host__ __device__ __forceinline__ WorkSlot work_slot(int w, int n_items, int n_heads, int block) {
+  const int per_block = block * n_heads;
+  const int b = w / per_block;
+  const int base = b * block;
+  const int nb = n_items - base < block ? n_items - base : block;
+  const int r = w - b * per_block;
+  WorkSlot s;
+  s.head = r / nb;
+  s.pos = base + r % nb;
+  return s;
+}
+
 // --------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, uint64_t* bar, int c0,
                                             int c1, int c2) {
