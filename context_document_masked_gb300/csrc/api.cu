@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "kernels.h"
 #include "plan.h"
@@ -105,12 +106,6 @@ int check_dims(const fcp_dims& d, const Plan* p) {
   return FCP_OK;
 }
 
-int check_dev_plan(const fcp_dev_plan* dp, int32_t shard) {
-  if (!dp || !dp->host || !dp->base) return FCP_ERR_INVALID_ARG;
-  if (shard < -1 || shard >= dp->n_shards) return FCP_ERR_INVALID_ARG;
-  return FCP_OK;
-}
-
 float softmax_scale(const fcp_dims& d) { return d.scale > 0.f ? d.scale : 1.0f / std::sqrt((float)d.d); }
 
 int64_t remote_rows_of(const Plan* p, int32_t shard) {
@@ -121,7 +116,28 @@ int64_t remote_rows_of(const Plan* p, int32_t shard) {
 
 namespace fcp {
 int64_t wait_limit_ns() { return g_wait_ns; }
+
+// A device-plan handle must describe its host plan exactly: the kernels index
+// the device tables with these offsets and counts, so a handle that was
+// corrupted, hand-edited or bound to another plan is rejected before anything
+// is launched.
+int check_dev_plan(const fcp_dev_plan* dp, int32_t shard) {
+  if (!dp || !dp->host || !dp->base) return FCP_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(dp->base) & 15) != 0) return FCP_ERR_INVALID_ARG;
+  const Plan* p = dp->host;
+  if (dp->n_shards != p->N || (int64_t)dp->T != p->T || dp->total_remote_rows != p->total_remote ||
+      dp->bytes != (int64_t)p->dev.size() * 4)
+    return FCP_ERR_INVALID_ARG;
+  for (int t = 0; t < fcp::TB_COUNT; ++t)
+    if (dp->tables[t] != p->tab_off[t] || dp->counts[t] != p->tab_cnt[t]) return FCP_ERR_INVALID_ARG;
+  for (int t = fcp::TB_COUNT; t < 16; ++t)
+    if (dp->tables[t] != 0 || dp->counts[t] != 0) return FCP_ERR_INVALID_ARG;
+  if (shard < -1 || shard >= dp->n_shards) return FCP_ERR_INVALID_ARG;
+  return FCP_OK;
+}
 }  // namespace fcp
+
+using fcp::check_dev_plan;
 
 extern "C" {
 
@@ -134,6 +150,7 @@ const char* fcp_strerror(int s) {
     case FCP_ERR_TIMEOUT: return "bounded device wait expired";
     case FCP_ERR_INFEASIBLE: return "policy infeasible for this input";
     case FCP_ERR_CAPACITY: return "buffer too small";
+    case FCP_ERR_MISSING_PART: return "partial result missing or duplicated";
     default: return "unknown status";
   }
 }
@@ -309,7 +326,7 @@ int fcp_gather_kv(const void* k, const void* v, const fcp_dev_plan* plan, int32_
     shift = (int32_t)p->shards[shard].kbuf_base;
   }
   return fcp::launch_gather(k, v, table(plan, fcp::TB_COPY) + 4 * t0, t1 - t0, shift,
-                            (int64_t)hkv * d * 2, kbuf, vbuf, num_sms(),
+                            (int64_t)hkv * d * 2, kbuf, vbuf, plan->T, (int32_t)rows, num_sms(),
                             static_cast<cudaStream_t>(stream));
 }
 
@@ -409,6 +426,10 @@ static int attn_fwd_impl(const void* q, const void* k, const void* v, const void
   fp.work_counter = counter;
   fp.qk_scale = qk8 ? reinterpret_cast<const float*>(wsb + kQkScaleOff) : nullptr;
   fp.rescale_count = reinterpret_cast<int*>(wsb + kRescaleCountOff);
+  fp.n_tiles = plan->counts[fcp::TB_FTILES];
+  fp.n_pieces = plan->counts[ring_order ? fcp::TB_RPIECES : fcp::TB_PIECES];
+  fp.n_segs = plan->counts[ring_order ? fcp::TB_RSEGS : fcp::TB_SEGS];
+  fp.kb_rows = rrows > 0 ? (int32_t)rrows : dims.T;
   fp.wait_ns = g_wait_ns;
   a.d = dims.d;
   a.num_sms = num_sms();
@@ -468,6 +489,23 @@ int fcp_merge(const float* o_parts, const float* lse_parts, int32_t B, int64_t r
                            static_cast<cudaStream_t>(stream));
 }
 
+int fcp_merge_ring(const fcp_dev_plan* plan, const float* o_parts, const float* lse_parts,
+                   const int32_t* part_step, int32_t B, int32_t hq, int32_t d, void* out, float* lse_out,
+                   void* stream) {
+  int st = check_dev_plan(plan, -1);
+  if (st) return st;
+  if (!part_step && B > 0) return FCP_ERR_INVALID_ARG;
+  const int32_t N = plan->n_shards;
+  if (B != N) return FCP_ERR_MISSING_PART;
+  std::vector<uint8_t> seen(N, 0);
+  for (int32_t b = 0; b < B; ++b) {
+    const int32_t s = part_step[b];
+    if (s < 0 || s >= N || seen[s]) return FCP_ERR_MISSING_PART;
+    seen[s] = 1;
+  }
+  return fcp_merge(o_parts, lse_parts, B, plan->T, hq, d, out, lse_out, stream);
+}
+
 int fcp_attn_bwd(const void* q, const void* k, const void* v, const void* kbuf, const void* vbuf,
                  const void* out, int32_t out_dtype, const float* lse, const void* dout,
                  const fcp_dev_plan* plan, int32_t shard, fcp_dims dims, float* dq, float* dk,
@@ -498,7 +536,8 @@ int fcp_attn_bwd(const void* q, const void* k, const void* v, const void* kbuf, 
     r1 = host_at(p, fcp::TB_RSHARD, shard + 1);
   }
   st = fcp::launch_bwd_preprocess(out, out_dtype == FCP_OUT_F32, dout, q, table(plan, fcp::TB_ROWS),
-                                  table(plan, fcp::TB_IDENT) + r0, r1 - r0, dims.T, dims.hq, dims.d,
+                                  table(plan, fcp::TB_IDENT) + r0, r1 - r0, plan->counts[fcp::TB_ROWS], dims.T,
+                                  dims.hq, dims.d,
                                   delta, dq, q16, do16, static_cast<int*>(ws),
                                   reinterpret_cast<int*>(wsb + kWorkCounterOff), s);
   if (st) return st;
@@ -542,6 +581,8 @@ int fcp_attn_bwd(const void* q, const void* k, const void* v, const void* kbuf, 
   bp.dv = dv;
   bp.err = static_cast<int*>(ws);
   bp.work_counter = reinterpret_cast<int*>(wsb + kWorkCounterOff);
+  bp.n_tiles = plan->counts[fcp::TB_BTILES];
+  bp.kb_rows = rrows > 0 ? (int32_t)rrows : dims.T;
   bp.wait_ns = g_wait_ns;
   a.d = dims.d;
   a.num_sms = num_sms();
@@ -559,6 +600,7 @@ int fcp_get_device_status(void* ws, void* stream) {
   if (cudaStreamSynchronize(s) != cudaSuccess) return FCP_ERR_CUDA;
   if (word & 1) return FCP_ERR_TIMEOUT;
   if (word & 4) return FCP_ERR_UNSUPPORTED;  // an input exceeds the fp16 operand range
+  if (word & fcp::kErrBadTable) return FCP_ERR_INVALID_ARG;  // checked build: a table index out of range
   return FCP_ERR_CUDA;
 }
 

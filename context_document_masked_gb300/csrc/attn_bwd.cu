@@ -75,13 +75,26 @@ struct BwdCfg {
 
 struct BwdItem {
   int key0, n, src, src_row, qa0, qa_end, na, qb0, qb_end, nb, nq, g;
+  bool bad;  // checked build: the unit's table entries are out of range (skip it)
 };
+
+// Query tiles q0, q0 + 128, ... (n of them) lie inside [0, q_end] and q_end <= T.
+__device__ __forceinline__ bool qrange_ok(int q0, int q_end, int n, int T) {
+  return n == 0 || (n > 0 && q0 >= 0 && q_end <= T && (int64_t)q0 + (int64_t)(n - 1) * 128 < q_end);
+}
 
 __device__ __forceinline__ BwdItem decode(const BwdParams& p, int w) {
   const WorkSlot ws = work_slot(w, p.n_items, p.hkv, p.order_block);
   const int item = __ldg(p.order + ws.pos);
-  const int* t = p.tiles + kBwdTileInts * item;
   BwdItem it;
+  it.bad = false;
+  if constexpr (kDeviceChecks) {
+    if (item < 0 || item >= p.n_tiles) {
+      it = BwdItem{0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, true};
+      return it;
+    }
+  }
+  const int* t = p.tiles + kBwdTileInts * item;
   it.key0 = __ldg(t + 0);
   it.n = __ldg(t + 1);
   it.src = __ldg(t + 2);
@@ -94,6 +107,12 @@ __device__ __forceinline__ BwdItem decode(const BwdParams& p, int w) {
   it.nb = __ldg(t + 9);
   it.nq = it.na + it.nb;
   it.g = ws.head;
+  if constexpr (kDeviceChecks) {
+    const int rows = it.src ? p.kb_rows : p.T;
+    it.bad = it.n < 1 || it.n > 128 || it.key0 < 0 || it.key0 > p.T - it.n || (it.src != 0 && it.src != 1) ||
+             it.src_row < 0 || it.src_row > rows - it.n || !qrange_ok(it.qa0, it.qa_end, it.na, p.T) ||
+             !qrange_ok(it.qb0, it.qb_end, it.nb, p.T);
+  }
   return it;
 }
 
@@ -241,6 +260,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) w_next = next_work(p.work_counter);
       w_next = __shfl_sync(0xffffffffu, w_next, 0);
       const BwdItem it = decode(p, w);
+      if (it.bad) {  // checked build: skipped by every role
+        if (lane == 0) atomicOr(p.err, kErrBadTable);
+        w = w_next;
+        continue;
+      }
       if (kv_items > 0) {
         ok = mbar_wait(&bar_kv_empty, (kv_items - 1) & 1, wc);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -344,6 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ring.release(k);
         if (w >= n_work) break;
         const BwdItem it = decode(p, w);
+        if (it.bad) continue;
         const int nsteps = G * it.nq;
         if (!(ok = mbar_wait(&bar_kv_conv, kv_items & 1, wc))) break;
         tc_fence_after();
@@ -419,6 +444,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) ring.release(k);
       if (w >= n_work) break;
+      if constexpr (kDeviceChecks) {
+        if (decode(p, w).bad) continue;
+      }
       ok = mbar_wait(&bar_kv_full, items & 1, wc);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
 #pragma unroll 4
@@ -453,6 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) ring.release(k);
       if (w >= n_work) break;
       const BwdItem it = decode(p, w);
+      if (it.bad) continue;
       const int nsteps = G * it.nq;
       const bool key_valid = kr < it.n;
       const int key = it.key0 + kr;
@@ -621,6 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) ring.release(k);
       if (w >= n_work) break;
       const BwdItem it = decode(p, w);
+      if (it.bad) continue;
       const int nsteps = G * it.nq;
       for (int j = 0; j < nsteps; ++j, ++gstep) {
         const StepRows sr = step_rows(it, G, j);

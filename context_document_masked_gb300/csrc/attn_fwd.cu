@@ -108,11 +108,26 @@ struct Walker {
   }
 };
 
-__device__ __forceinline__ int count_key_tiles(const int32_t* segs, int seg_begin, int seg_count,
-                                               int q_last, int lo, int hi, int filter) {
+// A key segment's keys and source rows lie inside the sequence and inside
+// the tensor its source names (own K/V rows, or the received rows behind
+// tm_kb, `shift` rows into them). Checked build only.
+__device__ __forceinline__ bool segment_ok(const FwdParams& p, const int* g) {
+  const int src = __ldg(g + 0), row = __ldg(g + 1) - (__ldg(g + 0) ? p.kbuf_shift : 0);
+  const int ks = __ldg(g + 2), len = __ldg(g + 3);
+  const int rows = src ? p.kb_rows : p.T;
+  return len >= 0 && ks >= 0 && ks <= p.T - len && row >= 0 && row <= rows - len;
+}
+
+// Key tiles a query tile visits; -1 (checked build) if one of its segments
+// fails segment_ok.
+__device__ __forceinline__ int count_key_tiles(const FwdParams& p, const int32_t* segs, int seg_begin,
+                                               int seg_count, int q_last, int lo, int hi, int filter) {
   int n = 0;
   for (int s = seg_begin; s < seg_begin + seg_count; ++s) {
     const int* g = segs + 4 * s;
+    if constexpr (kDeviceChecks) {
+      if (!segment_ok(p, g)) return -1;
+    }
     const int ks = __ldg(g + 2);
     if (ks > q_last || (filter >= 0 && __ldg(g) != filter)) continue;
     const int a = max(ks, lo);
@@ -124,6 +139,7 @@ __device__ __forceinline__ int count_key_tiles(const int32_t* segs, int seg_begi
 
 struct WorkItem {
   int q_start, q_rows, seg_begin, seg_count, h0, h1, g;
+  bool bad;  // checked build: the unit's table entries are out of range (skip it)
 };
 
 // Head pairs per query tile: each GQA group's heads two at a time; an odd
@@ -137,13 +153,30 @@ __device__ __forceinline__ WorkItem decode(const FwdParams& p, int w) {
   const WorkSlot ws = work_slot(w, p.n_items, hp_count, p.order_block);
   const int item = __ldg(p.order + ws.pos);
   const int hp = ws.head;
+  WorkItem it;
+  it.bad = false;
+  if constexpr (kDeviceChecks) {
+    if (item < 0 || item >= p.n_tiles) {
+      it = WorkItem{0, 0, 0, 0, 0, 0, 0, true};
+      return it;
+    }
+  }
   const int* t = p.tiles + 4 * item;
   const int piece = __ldg(t + 0);
-  WorkItem it;
+  if constexpr (kDeviceChecks) {
+    if (piece < 0 || piece >= p.n_pieces) {
+      it = WorkItem{0, 0, 0, 0, 0, 0, 0, true};
+      return it;
+    }
+  }
   it.q_start = __ldg(t + 1);
   it.q_rows = __ldg(t + 2);
   it.seg_begin = __ldg(p.pieces + 8 * piece + 5);
   it.seg_count = __ldg(p.pieces + 8 * piece + 6);
+  if constexpr (kDeviceChecks) {
+    it.bad = it.q_rows < 1 || it.q_rows > 128 || it.q_start < 0 || it.q_start > p.T - it.q_rows ||
+             it.seg_begin < 0 || it.seg_count < 0 || it.seg_begin > p.n_segs - it.seg_count;
+  }
   if constexpr (ODD) {
     const int G = p.hq / p.hkv, per_group = (G + 1) / 2;
     it.g = hp / per_group;
@@ -228,8 +261,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = ring.put<true>(k++, w, wc)) || w >= n_work) break;
         const WorkItem it = decode<ODD>(p, w);
         const int q_last = it.q_start + it.q_rows - 1;
-        const int nt = count_key_tiles(p.segs, it.seg_begin, it.seg_count, q_last, p.kv_lo, p.kv_hi, p.seg_filter);
-        if (nt == 0) continue;
+        const int nt = it.bad ? -1 : count_key_tiles(p, p.segs, it.seg_begin, it.seg_count, q_last, p.kv_lo, p.kv_hi, p.seg_filter);
+        if (nt < 0) atomicOr(p.err, kErrBadTable);
+        if (nt <= 0) continue;
         if (q_iter > 0 && !(ok = mbar_wait_inline(&bar_q_empty, (q_iter - 1) & 1, wc))) break;
         if constexpr (QK8) {  // e4m3 rows of D bytes: one box per head
           mbar_arrive_expect_tx(&bar_q_full, 2 * 128 * D);
@@ -313,8 +347,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (w >= n_work) break;
         const WorkItem it = decode<ODD>(p, w);
         const int q_last = it.q_start + it.q_rows - 1;
-        const int nt = count_key_tiles(p.segs, it.seg_begin, it.seg_count, q_last, p.kv_lo, p.kv_hi, p.seg_filter);
-        if (nt == 0) continue;
+        const int nt = it.bad ? -1 : count_key_tiles(p, p.segs, it.seg_begin, it.seg_count, q_last, p.kv_lo, p.kv_hi, p.seg_filter);
+        if (nt <= 0) continue;
         if (!(ok = mbar_wait_inline(&bar_q_full, q_iter & 1, wc))) break;
         tc_fence_after();
         // S_0, S_1 of the first key tile.
@@ -385,7 +419,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (w >= n_work) break;
       const WorkItem it = decode<ODD>(p, w);
       const int q_last = it.q_start + it.q_rows - 1;
-      const int nt = count_key_tiles(p.segs, it.seg_begin, it.seg_count, q_last, p.kv_lo, p.kv_hi, p.seg_filter);
+      const int nt = it.bad ? -1 : count_key_tiles(p, p.segs, it.seg_begin, it.seg_count, q_last, p.kv_lo, p.kv_hi, p.seg_filter);
+      if (nt < 0) continue;  // checked build: a unit with out-of-range table entries stores nothing
       const int q = it.q_start + r;
       bool row_valid = r < it.q_rows;
       int head = it.h0 + i;

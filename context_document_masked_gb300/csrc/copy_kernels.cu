@@ -37,11 +37,17 @@ constexpr int kGatherUnroll = 4;
 __global__ void __launch_bounds__(kGatherThreads)
     gather_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
                   const int32_t* __restrict__ tasks, int32_t n_tasks, int32_t dst_shift,
-                  int64_t row_vecs, uint4* __restrict__ kbuf, uint4* __restrict__ vbuf) {
+                  int64_t row_vecs, uint4* __restrict__ kbuf, uint4* __restrict__ vbuf, int32_t src_rows,
+                  int32_t dst_rows) {
   for (int t = blockIdx.x; t < n_tasks; t += gridDim.x) {
     const int src = __ldg(tasks + 4 * t + 0);
     const int dst = __ldg(tasks + 4 * t + 1) - dst_shift;
     const int nrows = __ldg(tasks + 4 * t + 2);
+    // Checked build: a run outside K/V or outside the destination buffer is
+    // skipped (the call has no error word; the attention kernels that read
+    // the same plan report such tables).
+    if (kDeviceChecks && (nrows < 0 || src < 0 || src > src_rows - nrows || dst < 0 || dst > dst_rows - nrows))
+      continue;
     const int64_t n = (int64_t)nrows * row_vecs;
     const uint4* ks = k + (int64_t)src * row_vecs;
     const uint4* vs = v + (int64_t)src * row_vecs;
@@ -172,7 +178,7 @@ template <int D, bool OF32>
 __global__ void __launch_bounds__(kPreThreads)
     preprocess_kernel(const void* __restrict__ out, const __nv_bfloat16* __restrict__ dout,
                       const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ rows,
-                      const int32_t* __restrict__ order, int n_chunks, int T, int hq,
+                      const int32_t* __restrict__ order, int n_chunks, int n_rows_table, int T, int hq,
                       float* __restrict__ delta, float* __restrict__ dq, __half* __restrict__ q16,
                       __half* __restrict__ do16, int* __restrict__ err, int* __restrict__ zero_word) {
   if (zero_word && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *zero_word = 0;
@@ -185,7 +191,19 @@ __global__ void __launch_bounds__(kPreThreads)
   bool ovf = false;
   for (int c = blockIdx.x; c < n_chunks; c += gridDim.x) {
     const int chunk = __ldg(order + c);
+    if constexpr (kDeviceChecks) {
+      if (chunk < 0 || chunk >= n_rows_table) {
+        if (threadIdx.x == 0) atomicOr(err, kErrBadTable);
+        continue;
+      }
+    }
     const int r0 = __ldg(rows + 2 * chunk), nr = __ldg(rows + 2 * chunk + 1);
+    if constexpr (kDeviceChecks) {
+      if (nr < 0 || r0 < 0 || r0 > T - nr) {
+        if (threadIdx.x == 0) atomicOr(err, kErrBadTable);
+        continue;
+      }
+    }
     const int total = nr * hq * L;  // 16-byte groups of the chunk
     const int64_t e0 = (int64_t)r0 * hq * D;
     // Warp-uniform trip count: every lane of a warp takes part in the
@@ -380,13 +398,13 @@ int launch_round_bf16(const float* src, void* dst, int64_t n_elems, int num_sms,
 }
 
 int launch_gather(const void* k, const void* v, const int32_t* tasks, int32_t n_tasks,
-                  int32_t dst_shift, int64_t row_bytes, void* kbuf, void* vbuf, int num_sms,
-                  cudaStream_t st) {
+                  int32_t dst_shift, int64_t row_bytes, void* kbuf, void* vbuf, int32_t src_rows,
+                  int32_t dst_rows, int num_sms, cudaStream_t st) {
   if (n_tasks == 0) return FCP_OK;
   const int grid = n_tasks < num_sms * 8 ? n_tasks : num_sms * 8;
   gather_kernel<<<grid, kGatherThreads, 0, st>>>(
       static_cast<const uint4*>(k), static_cast<const uint4*>(v), tasks, n_tasks, dst_shift,
-      row_bytes / 16, static_cast<uint4*>(kbuf), static_cast<uint4*>(vbuf));
+      row_bytes / 16, static_cast<uint4*>(kbuf), static_cast<uint4*>(vbuf), src_rows, dst_rows);
   return cudaGetLastError() == cudaSuccess ? FCP_OK : FCP_ERR_CUDA;
 }
 
@@ -426,7 +444,8 @@ int launch_merge(const float* o_parts, const float* lse_parts, int32_t B, int64_
 }
 
 int launch_bwd_preprocess(const void* out, bool out_f32, const void* dout, const void* q,
-                          const int32_t* rows, const int32_t* order, int32_t n_chunks, int32_t T,
+                          const int32_t* rows, const int32_t* order, int32_t n_chunks, int32_t n_rows_table,
+                          int32_t T,
                           int32_t hq, int32_t d, float* delta, float* dq, void* q16, void* do16,
                           int* err, int* zero_word, cudaStream_t st) {
   if (n_chunks == 0 && !zero_word) return FCP_OK;
@@ -434,7 +453,7 @@ int launch_bwd_preprocess(const void* out, bool out_f32, const void* dout, const
   using B = __nv_bfloat16;
   auto go = [&](auto kernel) {
     kernel<<<grid, kPreThreads, 0, st>>>(out, static_cast<const B*>(dout), static_cast<const B*>(q),
-                                         rows, order, n_chunks, T, hq, delta, dq,
+                                         rows, order, n_chunks, n_rows_table, T, hq, delta, dq,
                                          static_cast<__half*>(q16), static_cast<__half*>(do16), err,
                                          zero_word);
   };

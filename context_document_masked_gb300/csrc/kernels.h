@@ -7,7 +7,19 @@
 
 #include "../../include/fcp.h"
 
+// FCP_DEVICE_CHECKS=1 builds the checked library: every index the kernels
+// read from the plan's device tables is checked against the table sizes and
+// the tensors' rows before use; a failed check sets bit kErrBadTable of the
+// error word (fcp_get_device_status: FCP_ERR_INVALID_ARG) and the kernel
+// skips that work unit. It never traps.
+#ifndef FCP_DEVICE_CHECKS
+#define FCP_DEVICE_CHECKS 0
+#endif
+
 namespace fcp {
+
+constexpr bool kDeviceChecks = FCP_DEVICE_CHECKS != 0;
+constexpr int kErrBadTable = 8;
 
 // Ints per backward unit in the plan's TB_BTILES table.
 constexpr int kBwdTileInts = 12;
@@ -31,6 +43,7 @@ struct FwdParams {
   const float* qk_scale;   // e4m3 Q K^T variant: the scales 2^kq, 2^kk of Q and K (else unused)
   int* rescale_count;      // if not null: +1 per warp each time O is rescaled after a later key tile
   int32_t order_block;     // work decode: items per block (set by the launch, see work_slot)
+  int32_t n_tiles, n_pieces, n_segs, kb_rows;  // table sizes, rows behind tm_kb (checked build)
   int64_t wait_ns;
 };
 
@@ -59,6 +72,7 @@ struct BwdParams {
   int* err;
   int* work_counter;       // zero at launch (set by the preprocess)
   int32_t order_block;     // work decode: items per block (set by the launch, see work_slot)
+  int32_t n_tiles, kb_rows;  // TB_BTILES size, rows behind tm_kb/tm_vb (checked build)
   int64_t wait_ns;
 };
 
@@ -81,9 +95,11 @@ int64_t wait_limit_ns();
 // rows set to zero, and fp16 copies of Q and dO for the backward's MMAs.
 // *zero_word (if not null) is set to 0: the work counter of the kernel that
 // follows in the same stream.
+// n_rows_table: entries of `rows` (the checked build bounds the chunk indices).
 int launch_bwd_preprocess(const void* out, bool out_f32, const void* dout, const void* q,
                           const int32_t* rows,
-                          const int32_t* order, int32_t n_chunks, int32_t T, int32_t hq, int32_t d,
+                          const int32_t* order, int32_t n_chunks, int32_t n_rows_table, int32_t T, int32_t hq,
+                          int32_t d,
                           float* delta, float* dq, void* q16, void* do16, int* err, int* zero_word,
                           cudaStream_t st);
 
@@ -107,10 +123,11 @@ int launch_quant_e4m3(const void* src, void* dst, int64_t n_elems, unsigned* ama
 int launch_quant_e4m3_with(const void* src, void* dst, int64_t n_elems, const unsigned* amax_bits,
                            int num_sms, cudaStream_t st);
 
-// Gather of received KV rows: tasks (src_row, dst_row, nrows, shard).
+// Gather of received KV rows: tasks (src_row, dst_row, nrows, shard); K/V
+// hold src_rows rows, kbuf/vbuf dst_rows (bounds of the checked build).
 int launch_gather(const void* k, const void* v, const int32_t* tasks, int32_t n_tasks,
-                  int32_t dst_shift, int64_t row_bytes, void* kbuf, void* vbuf, int num_sms,
-                  cudaStream_t st);
+                  int32_t dst_shift, int64_t row_bytes, void* kbuf, void* vbuf, int32_t src_rows,
+                  int32_t dst_rows, int num_sms, cudaStream_t st);
 
 int launch_merge(const float* o_parts, const float* lse_parts, int32_t B, int64_t rows, int32_t hq,
                  int32_t d, void* out, float* lse_out, int num_sms, cudaStream_t st);

@@ -96,8 +96,7 @@ extern "C" int fcp_attn_fwd_noalloc(const void* q, const void* k, const void* v,
                                     const void* vbuf, const fcp_dev_plan* plan, int32_t shard,
                                     int32_t kv_lo, int32_t kv_hi, fcp_dims dims, int32_t out_dtype,
                                     void* out, float* lse, void* stream) {
-  if (!plan || !plan->host || !plan->base) return FCP_ERR_INVALID_ARG;
-  if (shard < -1 || shard >= plan->n_shards) return FCP_ERR_INVALID_ARG;
+  if (int st0 = fcp::check_dev_plan(plan, shard)) return st0;
   const fcp::Plan* p = plan->host;
   if (dims.T <= 0 || dims.hq <= 0 || dims.hkv <= 0 || dims.T != p->T) return FCP_ERR_INVALID_ARG;
   if (dims.d != 64 && dims.d != 128) return FCP_ERR_UNSUPPORTED;
@@ -176,6 +175,10 @@ extern "C" int fcp_attn_fwd_noalloc(const void* q, const void* k, const void* v,
   fp.err = err;
   fp.work_counter = counter;
   fp.rescale_count = nullptr;
+  fp.n_tiles = plan->counts[fcp::TB_FTILES];
+  fp.n_pieces = plan->counts[fcp::TB_PIECES];
+  fp.n_segs = plan->counts[fcp::TB_SEGS];
+  fp.kb_rows = rrows > 0 ? (int32_t)rrows : dims.T;
   fp.wait_ns = fcp::wait_limit_ns();
   a.d = dims.d;
   a.num_sms = num_sms();

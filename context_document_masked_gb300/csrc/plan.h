@@ -79,4 +79,9 @@ struct fcp_plan : fcp::Plan {};
 namespace fcp {
 int make_plan(const int32_t* doclens, int32_t n_docs, int32_t cp, int32_t policy, double R,
               fcp_plan_t** out);
+
+// FCP_OK if `dp` describes its host plan exactly (table offsets, counts, sizes,
+// a 16-byte aligned base) and -1 <= shard < the plan's shard count;
+// FCP_ERR_INVALID_ARG otherwise. Host only, no CUDA call.
+int check_dev_plan(const fcp_dev_plan* dp, int32_t shard);
 }  // namespace fcp

@@ -12,9 +12,13 @@ import os
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "_lib", "libfcp.so")
+# FCP_DEVICE_CHECKS=1 selects the checked build (device-side bounds checks on
+# every plan-table index; build with build.build(checked=True)).
+CHECKED = os.environ.get("FCP_DEVICE_CHECKS") == "1"
+LIB_PATH = os.path.join(_HERE, "_lib_checked" if CHECKED else "_lib", "libfcp.so")
 
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_INFEASIBLE, ERR_CAPACITY = range(7)
+(OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_INFEASIBLE, ERR_CAPACITY,
+ ERR_MISSING_PART) = range(8)
 POLICIES = {"llama3": 0, "perdoc": 1, "wholedoc": 2, "hybrid": 3, "hybrid_tiles": 4}
 OUT_BF16, OUT_F32 = 0, 1
 
@@ -24,7 +28,7 @@ EXPORTED = (
     "fcp_workspace_bytes", "fcp_gather_kv", "fcp_attn_fwd", "fcp_merge", "fcp_attn_bwd",
     "fcp_get_device_status", "fcp_debug_set_wait_limit", "fcp_attn_fwd_noalloc", "fcp_attn_fwd_ring",
     "fcp_attn_fwd_qk8", "fcp_quant_e4m3", "fcp_plan_device_image", "fcp_plan_bind",
-    "fcp_debug_rescale_events", "fcp_round_bf16",
+    "fcp_debug_rescale_events", "fcp_round_bf16", "fcp_merge_ring",
 )
 
 
@@ -106,6 +110,8 @@ def _load():
         "fcp_debug_set_wait_limit": (None, [i64]),
         "fcp_debug_rescale_events": (C.c_int, [vp, vp, C.POINTER(i64)]),
         "fcp_round_bf16": (C.c_int, [vp, i64, vp, vp]),
+        "fcp_merge_ring": (C.c_int, [C.POINTER(DevPlan), vp, vp, C.POINTER(C.c_int32), i32, i32, i32, vp, vp,
+                                     vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -338,6 +344,19 @@ def merge(o_parts, lse_parts, out, lse_out, stream=None):
     B, rows, hq, d = o_parts.shape
     _check(_lib.fcp_merge(_ptr(o_parts), _ptr(lse_parts), B, rows, hq, d, _ptr(out), _ptr(lse_out),
                           _stream(stream)), "fcp_merge")
+
+
+def merge_ring(dplan: DevicePlan, o_parts, lse_parts, part_step, out, lse_out, stream=None):
+    """fcp_merge_ring: merge of the N ring-step partials; part_step[b] is the
+    ring step that produced partial b (a missing or duplicated step raises
+    FcpError with status ERR_MISSING_PART before anything is launched)."""
+    B, rows, hq, d = o_parts.shape
+    steps = np.ascontiguousarray(np.asarray(part_step, dtype=np.int32))
+    if len(steps) != B or rows != dplan.c.T or tuple(lse_parts.shape) != (B, hq, rows):
+        raise ValueError("merge_ring: one step tag per partial, each partial [T][hq][d] with T the plan's")
+    _check(_lib.fcp_merge_ring(C.byref(dplan.c), _ptr(o_parts), _ptr(lse_parts),
+                               steps.ctypes.data_as(C.POINTER(C.c_int32)), len(steps), hq, d, _ptr(out),
+                               _ptr(lse_out), _stream(stream)), "fcp_merge_ring")
 
 
 def attn_bwd(q, k, v, kbuf, vbuf, out, lse, dout, dplan: DevicePlan, shard: int, dq, dk, dv, ws,

@@ -29,6 +29,29 @@ class CPAttention:
         ws_bytes = fcp.workspace_bytes(self.dims, self.plan)
         self.ws = torch.zeros(ws_bytes // 4, dtype=torch.int32, device=self.device)
 
+    def set_plan(self, doclens, target_imbalance: float = 1.05, stream=None):
+        """A new plan for the next packed sequence (same T, CP size, policy and
+        shapes), uploaded into this session's plan buffer on `stream`; the
+        received-key buffers and the workspace are kept when they are large
+        enough and replaced otherwise. The previous plan's tables must no longer
+        be in use by queued work on other streams."""
+        plan = fcp.Plan(doclens, self.cp, self.plan.policy, target_imbalance)
+        if int(sum(int(x) for x in doclens)) != self.T:
+            raise ValueError("set_plan: the token count differs from the session's")
+        nbytes = plan.device_bytes()
+        if self.plan_buf.numel() * 4 < nbytes:
+            self.plan_buf = torch.empty(nbytes // 4, dtype=torch.int32, device=self.device)
+        self.plan = plan
+        self.dplan = plan.upload(self.plan_buf, stream=stream)
+        rows = max(1, self.dplan.total_remote_rows)
+        if self.kbuf.shape[0] < rows:
+            self.kbuf = torch.empty(rows, self.hkv, self.d, dtype=torch.bfloat16, device=self.device)
+            self.vbuf = torch.empty_like(self.kbuf)
+        ws_bytes = fcp.workspace_bytes(self.dims, plan)
+        if self.ws.numel() * 4 < ws_bytes:
+            self.ws = torch.zeros(ws_bytes // 4, dtype=torch.int32, device=self.device)
+        return self.dplan
+
     def stats(self) -> dict:
         return self.plan.stats()
 

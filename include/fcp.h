@@ -43,7 +43,8 @@ enum {
   FCP_ERR_CUDA = 3,          /* a CUDA runtime call failed                     */
   FCP_ERR_TIMEOUT = 4,       /* a bounded device wait expired (see status)     */
   FCP_ERR_INFEASIBLE = 5,    /* the policy cannot shard this input (e.g. T%2N) */
-  FCP_ERR_CAPACITY = 6       /* a caller buffer is too small                   */
+  FCP_ERR_CAPACITY = 6,      /* a caller buffer is too small                   */
+  FCP_ERR_MISSING_PART = 7   /* a partial result is missing or duplicated      */
 };
 
 enum {
@@ -340,6 +341,26 @@ int fcp_attn_fwd_ring(const void* q, const void* k, const void* v, const fcp_dev
  */
 int fcp_merge(const float* o_parts, const float* lse_parts, int32_t B, int64_t rows,
               int32_t hq, int32_t d, void* out, float* lse_out, void* stream);
+
+/*
+ * fcp_merge_ring -- fcp_merge of the N ring-step partials of a plan, with the
+ * check a distributed merge needs before it combines anything ([CPGuide]
+ * "Ring Attention": shard j folds in the partial of every ring step; the
+ * guide's go-live checklist asks that a lost or faulty rank be reported, not
+ * silently absorbed). The partials are those of fcp_attn_fwd_ring(ring_step =
+ * s) for every shard at once, fp32, one per step; part_step[b] (host) names
+ * the ring step that produced partial b -- in a distributed run, the tag each
+ * received partial carries.
+ *   o_parts   fp32 [B][T][hq][d]; lse_parts fp32 [B][hq][T] (T = the plan's).
+ *   out       bf16 [T][hq][d]; lse_out fp32 [hq][T].
+ * Errors, all before any launch: FCP_ERR_MISSING_PART unless B equals the
+ * plan's shard count N and part_step holds every step 0..N-1 exactly once (a
+ * lost partial, a duplicated one, or a tag outside the ring); the errors of
+ * fcp_merge otherwise.
+ */
+int fcp_merge_ring(const fcp_dev_plan* plan, const float* o_parts, const float* lse_parts,
+                   const int32_t* part_step, int32_t B, int32_t hq, int32_t d, void* out,
+                   float* lse_out, void* stream);
 
 /*
  * fcp_attn_bwd -- exact gradient of fcp_attn_fwd (full key set) for one shard

@@ -136,3 +136,40 @@ def test_ring_rejects_bad_step(cuda):
     for bad in (-2, cp):
         with pytest.raises(fcp.FcpError):
             s.forward_ring(qd, kd, vd, ring_step=bad)
+
+
+def test_merge_ring_checks_the_partials_and_matches_merge(cuda):
+    """fcp_merge_ring: with every ring step's partial present (tags in any
+    order) it equals fcp_merge of the same partials bit for bit and the
+    oracle; with one step's partial lost it reports FCP_ERR_MISSING_PART and
+    leaves the outputs untouched."""
+    from context_document_masked_gb300 import fcp
+    name, D, hq, hkv, d, cp, pol = CASES[1]
+    s, cu, q, k, v = _setup(*CASES[1])
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    order = [2, 0, 3, 1]                      # the order the partials "arrived" in
+    o_parts = torch.empty(cp, s.T, hq, d, dtype=torch.float32, device="cuda")
+    l_parts = torch.empty(cp, hq, s.T, dtype=torch.float32, device="cuda")
+    for b, st in enumerate(order):
+        s.forward_ring(qd, kd, vd, ring_step=st, out=o_parts[b], lse=l_parts[b], out_dtype=torch.float32)
+    out = torch.full((s.T, hq, d), 7.0, dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((hq, s.T), 7.0, dtype=torch.float32, device="cuda")
+    with pytest.raises(fcp.FcpError) as e:          # the partial of step 1 never arrived
+        fcp.merge_ring(s.dplan, o_parts[:3], l_parts[:3], order[:3], out, lse)
+    assert e.value.status == fcp.ERR_MISSING_PART
+    with pytest.raises(fcp.FcpError) as e:          # step 0 twice, step 1 lost
+        fcp.merge_ring(s.dplan, o_parts, l_parts, [2, 0, 3, 0], out, lse)
+    assert e.value.status == fcp.ERR_MISSING_PART
+    torch.cuda.synchronize()
+    assert bool((out == 7.0).all()) and bool((lse == 7.0).all())
+    fcp.merge_ring(s.dplan, o_parts, l_parts, order, out, lse)
+    ref_o = torch.empty_like(out)
+    ref_l = torch.empty_like(lse)
+    fcp.merge(o_parts, l_parts, ref_o, ref_l)
+    torch.cuda.synchronize()
+    assert s.device_status() == 0
+    assert torch.equal(out, ref_o) and torch.equal(lse, ref_l)
+    o_ref, lse_ref = A.attention_per_doc(q, k, v, cu)
+    half_ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(o_ref), 1e-30))) - 8)
+    assert float((np.abs(out.float().cpu().numpy() - o_ref) - half_ulp).max()) <= TOL_O
+    assert _err(lse.cpu(), lse_ref) <= TOL_LSE
