@@ -255,6 +255,80 @@ def attention_bwd_per_doc(q, k, v, o, lse, do, cu, scale=None, docs=None,
     return dq, dk, dv
 
 
+def _row_softmax(qi, kd, scale):
+    """Probabilities and log-sum-exp of one query row over the keys kd."""
+    s = scale * (kd @ qi)
+    m = s.max()
+    e = np.exp(s - m)
+    total = e.sum()
+    return e / total, m + math.log(total)
+
+
+def attention_bwd_query_rows(q, k, v, do, cu, rows, heads, scale=None, q_offset=0):
+    """dQ at sampled query rows, from the definition of the gradient row by
+    row (for spot checks at sizes where whole documents are too costly):
+    with the row's keys j in its document up to i,
+      P_ij = exp(s_ij - LSE_i), O_i = sum_j P_ij v_j, D_i = <dO_i, O_i>,
+      dS_ij = P_ij (<dO_i, v_j> - D_i),  dQ_i = scale sum_j dS_ij k_j.
+    q and do hold rows q_offset, q_offset + 1, ... of the sequence (all rows
+    when q_offset = 0); k, v and cu describe the whole sequence.
+    Returns dq [len(rows), len(heads), d] (fp64)."""
+    k, v = to_f64(k), to_f64(v)
+    _, Hq, d = q.shape
+    G = _group(Hq, k.shape[1])
+    scale = default_scale(d) if scale is None else scale
+    cu = np.asarray(cu, dtype=np.int64)
+    doc = doc_ids(cu)
+    dq = np.zeros((len(rows), len(heads), d))
+    for a, i in enumerate(np.asarray(rows, dtype=np.int64)):
+        s0 = int(cu[doc[i]])
+        qi, doi = to_f64(q[i - q_offset]), to_f64(do[i - q_offset])
+        for b, h in enumerate(heads):
+            g = h // G
+            kd, vd = k[s0:i + 1, g], v[s0:i + 1, g]
+            p, _ = _row_softmax(qi[h], kd, scale)
+            Di = float(doi[h] @ (p @ vd))
+            ds = p * (vd @ doi[h] - Di)
+            dq[a, b] = scale * (ds @ kd)
+    return dq
+
+
+def attention_bwd_key_rows(q, k, v, do, cu, key_rows, scale=None, q_offset=0):
+    """dK and dV at sampled key rows j (every KV head), from the definition:
+    every query i >= j of j's document and every query head h of the KV
+    head's group contribute
+      dV_j += P_ij dO_i,  dK_j += scale dS_ij q_i,
+    with P_ij, D_i and dS_ij as in attention_bwd_query_rows (each query row's
+    softmax over its own keys recomputed here). Costs O((doc end - j) * i * d)
+    per head: meant for key rows near the end of their document. q and do
+    hold rows q_offset, q_offset + 1, ... of the sequence, which must include
+    every query row from the first key row to its document's end.
+    Returns dk, dv [len(key_rows), Hkv, d] (fp64)."""
+    q, k, v, do = to_f64(q), to_f64(k), to_f64(v), to_f64(do)
+    _, Hq, d = q.shape
+    Hkv = k.shape[1]
+    G = _group(Hq, Hkv)
+    scale = default_scale(d) if scale is None else scale
+    cu = np.asarray(cu, dtype=np.int64)
+    doc = doc_ids(cu)
+    dk = np.zeros((len(key_rows), Hkv, d))
+    dv = np.zeros((len(key_rows), Hkv, d))
+    for a, j in enumerate(np.asarray(key_rows, dtype=np.int64)):
+        s0, s1 = int(cu[doc[j]]), int(cu[doc[j] + 1])
+        for h in range(Hq):
+            g = h // G
+            for i in range(j, s1):
+                kd, vd = k[s0:i + 1, g], v[s0:i + 1, g]
+                qi, doi = q[i - q_offset, h], do[i - q_offset, h]
+                p, _ = _row_softmax(qi, kd, scale)
+                Di = float(doi @ (p @ vd))
+                pj = p[j - s0]
+                dsj = pj * (float(v[j, g] @ doi) - Di)
+                dv[a, g] += pj * doi
+                dk[a, g] += scale * dsj * qi
+    return dk, dv
+
+
 def merge(o_parts, lse_parts):
     """Merge B partial results over disjoint key sets.
 

@@ -4,10 +4,12 @@ backward).
 
 The fp64 oracle cannot recompute these sizes whole, so it checks samples it
 can compute one by one: random query rows of every document (all heads) for
-O and LSE, and complete documents short enough for the exact per-document
-gradient for dQ, dK and dV. Documents are independent under the document
-mask, so a document's slice of the inputs determines its slice of every
-output. Tolerances as in test_gpu_attention.py.
+O and LSE; dQ at sampled query rows and dK, dV at the last key rows of every
+document, long ones included (the gradient's definition row by row); and
+complete documents short enough for the exact per-document gradient.
+Documents are independent under the document mask, so a document's slice of
+the inputs determines its slice of every output. Tolerances as in
+test_gpu_attention.py.
 """
 import numpy as np
 import pytest
@@ -21,7 +23,8 @@ pytestmark = pytest.mark.gpu
 TOL_O, TOL_LSE, TOL_GRAD = 1e-2, 1e-3, 1e-2
 
 
-def _run(cfg, policy=None, merge_blocks=0, bwd=True, rows_per_doc=6, max_bwd_doc=2100, seed=0):
+def _run(cfg, policy=None, merge_blocks=0, bwd=True, rows_per_doc=6, max_bwd_doc=2100, seed=0,
+         key_rows_per_doc=3):
     from context_document_masked_gb300 import fcp
     from context_document_masked_gb300.session import CPAttention
     w = synth.WORKLOADS[cfg]
@@ -55,12 +58,13 @@ def _run(cfg, policy=None, merge_blocks=0, bwd=True, rows_per_doc=6, max_bwd_doc
     assert s.device_status() == 0
     cu = synth.cu_from_lengths(D)
     rng = np.random.default_rng(seed + cfg)
-    errs = {"O": 0.0, "LSE": 0.0, "O_bf16_excess": 0.0, "merge": 0.0, "dQ": 0.0, "dK": 0.0, "dV": 0.0}
+    errs = {"O": 0.0, "LSE": 0.0, "O_bf16_excess": 0.0, "merge": 0.0, "dQ": 0.0, "dK": 0.0, "dV": 0.0,
+            "dQ_rows": 0.0, "dK_rows": 0.0, "dV_rows": 0.0}
     heads = list(range(hq))
     for i, L in enumerate(D):
         s0, s1 = int(cu[i]), int(cu[i + 1])
         local = sorted(set([0, L - 1] + rng.integers(0, L, size=rows_per_doc).tolist()))
-        ks, vs = k[s0:s1].cpu(), v[s0:s1].cpu()
+        ks, vs = A.to_f64(k[s0:s1]), A.to_f64(v[s0:s1])      # upcast once per document
         cu_l = np.array([0, L])
         o_r, l_r = A.attention_rows(q[[s0 + r for r in local]].cpu(), ks, vs, cu_l, local, heads,
                                     q_holds_rows=True)
@@ -77,6 +81,20 @@ def _run(cfg, policy=None, merge_blocks=0, bwd=True, rows_per_doc=6, max_bwd_doc
             g_m = merged[0][rows].cpu().double().numpy()
             errs["merge"] = max(errs["merge"], float((np.abs(g_m - o_r) - half_ulp).max()))
             errs["LSE"] = max(errs["LSE"], float(np.abs(merged[1][:, rows].cpu().double().numpy() - l_r).max()))
+        if grads is not None:
+            # dQ at two sampled rows and the last row; dK, dV at the last key rows.
+            for r in sorted(set([L - 1] + rng.integers(0, L, size=2).tolist())):
+                dq_r = A.attention_bwd_query_rows(q[s0 + r:s0 + r + 1].cpu(), ks, vs, do[s0 + r:s0 + r + 1].cpu(),
+                                                  cu_l, [r], heads, q_offset=r)
+                g = grads[0][s0 + r:s0 + r + 1].cpu().double().numpy()
+                errs["dQ_rows"] = max(errs["dQ_rows"], float(np.abs(g - dq_r).max()))
+            kr0 = max(0, L - key_rows_per_doc)
+            dk_r, dv_r = A.attention_bwd_key_rows(q[s0 + kr0:s1].cpu(), ks, vs, do[s0 + kr0:s1].cpu(), cu_l,
+                                                  list(range(kr0, L)), q_offset=kr0)
+            errs["dK_rows"] = max(errs["dK_rows"], float(np.abs(grads[1][s0 + kr0:s1].cpu().double().numpy()
+                                                                - dk_r).max()))
+            errs["dV_rows"] = max(errs["dV_rows"], float(np.abs(grads[2][s0 + kr0:s1].cpu().double().numpy()
+                                                                - dv_r).max()))
         if grads is not None and L <= max_bwd_doc:
             qs, dos = q[s0:s1].cpu(), do[s0:s1].cpu()
             o_d, l_d = A.attention_per_doc(qs, ks, vs, cu_l)
@@ -87,6 +105,7 @@ def _run(cfg, policy=None, merge_blocks=0, bwd=True, rows_per_doc=6, max_bwd_doc
     assert errs["O"] <= TOL_O and errs["LSE"] <= TOL_LSE and errs["O_bf16_excess"] <= TOL_O
     assert errs["merge"] <= TOL_O
     assert errs["dQ"] <= TOL_GRAD and errs["dK"] <= TOL_GRAD and errs["dV"] <= TOL_GRAD
+    assert errs["dQ_rows"] <= TOL_GRAD and errs["dK_rows"] <= TOL_GRAD and errs["dV_rows"] <= TOL_GRAD
     return errs
 
 

@@ -256,3 +256,47 @@ def test_rows_sampler_matches_per_doc():
     os2, ls2 = A.attention_rows(q[rows], k, v, cu, rows, heads, q_holds_rows=True)
     np.testing.assert_array_equal(os2, os_)
     np.testing.assert_array_equal(ls2, ls)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 2), (3, 1), (2, 2)])
+def test_sampled_row_gradients_match_autograd(Hq, Hkv):
+    """The row-by-row gradient functions used for full-size spot checks
+    (dQ at sampled query rows, dK/dV at sampled key rows) equal torch
+    autograd of the brute-force document-masked attention at those rows,
+    including first and last rows of documents and 1-token documents."""
+    lengths = [1, 14, 3, 27, 2, 9]
+    T, d = sum(lengths), 8
+    cu, q, k, v = _inputs(lengths, Hq=Hq, Hkv=Hkv, d=d, seed=12)
+    do = synth.make_dout(T, Hq, d, seed=12)
+    qt, kt, vt = (x.double().requires_grad_(True) for x in (q, k, v))
+    _torch_ref_forward(qt, kt, vt, cu, Hq, Hkv).backward(do.double())
+    rows = [0, 1, 5, 14, 15, 17, 18, 30, 44, 45, 46, 47, T - 1]
+    dq = A.attention_bwd_query_rows(q, k, v, do, cu, rows, list(range(Hq)))
+    np.testing.assert_allclose(dq, qt.grad.numpy()[rows], atol=1e-11, rtol=0)
+    key_rows = [0, 1, 7, 14, 16, 17, 40, 44, 45, 46, T - 2, T - 1]
+    dk, dv = A.attention_bwd_key_rows(q, k, v, do, cu, key_rows)
+    np.testing.assert_allclose(dk, kt.grad.numpy()[key_rows], atol=1e-11, rtol=0)
+    np.testing.assert_allclose(dv, vt.grad.numpy()[key_rows], atol=1e-11, rtol=0)
+
+
+def test_sampled_row_gradients_with_a_scale():
+    """The same with a non-default softmax scale (central differences of the
+    per-row functions' loss would need the full forward; here the scale enters
+    autograd through scaled queries: attention(q * c / (1/sqrt(d))) at the
+    default scale equals attention(q) at scale c)."""
+    lengths = [5, 11]
+    T, Hq, Hkv, d = 16, 2, 1, 8
+    cu, q, k, v = _inputs(lengths, Hq=Hq, Hkv=Hkv, d=d, seed=13)
+    do = synth.make_dout(T, Hq, d, seed=13)
+    c = 0.3
+    factor = c * math.sqrt(d)
+    qt = (A.to_f64(q) * 1.0)
+    qs = torch.tensor(qt * factor, requires_grad=True)
+    kt, vt = (x.double().requires_grad_(True) for x in (k, v))
+    _torch_ref_forward(qs, kt, vt, cu, Hq, Hkv).backward(do.double())
+    rows = list(range(T))
+    dq = A.attention_bwd_query_rows(q, k, v, do, cu, rows, list(range(Hq)), scale=c)
+    np.testing.assert_allclose(dq, qs.grad.numpy() * factor, atol=1e-11, rtol=0)
+    dk, dv = A.attention_bwd_key_rows(q, k, v, do, cu, rows, scale=c)
+    np.testing.assert_allclose(dk, kt.grad.numpy(), atol=1e-11, rtol=0)
+    np.testing.assert_allclose(dv, vt.grad.numpy(), atol=1e-11, rtol=0)
