@@ -421,9 +421,12 @@ int fcp_attn_fwd_noalloc(const void* q, const void* k, const void* v, const void
 /*
  * fcp_get_device_status -- read the workspace error word (synchronizes the
  * stream). FCP_ERR_TIMEOUT if a bounded pipeline wait expired in a previous
- * call on this workspace; FCP_ERR_UNSUPPORTED if a backward input exceeded
- * the fp16 range of its tensor-core operands (|x| > 65504); FCP_OK otherwise.
- * Clears the word.
+ * call on this workspace; FCP_ERR_UNSUPPORTED if an input exceeded the fp16
+ * range of its tensor-core operands (|x| > 65504: V in the forward, Q, dO, K
+ * or V in the backward); FCP_ERR_INVALID_ARG if, in the checked build of the
+ * library (compiled with FCP_DEVICE_CHECKS=1), a kernel found a plan-table
+ * index out of range and skipped that work unit; FCP_OK otherwise. Clears
+ * the word.
  */
 int fcp_get_device_status(void* ws, void* stream);
 
