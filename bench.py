@@ -600,8 +600,8 @@ def _bench_shards(torch, dev):
 def _bench_e2e(args, D, w, seed, torch, fcp):
     """End to end through the public API, pipelined the way a training loop
     would run it: step i's inputs go host -> device on one stream while step
-    i-1 computes, and its results device -> host on a third stream while step
-    i+1 computes. Every step copies all of its inputs in (Q, K, V, dO bf16) and
+    i-1 computes (Q, K, V first, then dO, which only the backward reads), and
+    its results device -> host on a third stream while step i+1 computes. Every step copies all of its inputs in (Q, K, V, dO bf16) and
     all of its results out (O rounded to bf16 -- the forward keeps its fp32 O
     on the device for the backward's D_i -- and dQ, dK, dV fp32), builds its
     plan and allocates its session buffers; buffers alternate between two sets,
@@ -628,9 +628,12 @@ def _bench_e2e(args, D, w, seed, torch, fcp):
     s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     ev = lambda: torch.cuda.Event()  # noqa: E731
     in_ready, comp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    do_ready = [ev(), ev()]
     fwd_done = [ev(), ev()]
     pairs = sum(L * (L + 1) // 2 for L in D)
     sessions = [None, None]
+    marks = []   # (start, end) events of each step's kernels on the compute stream
+    cin, cout = [], []   # (start, end) events of each step's host->device / device->host copies
 
     def h2d(b):
         with torch.cuda.stream(s_in):
@@ -642,9 +645,17 @@ def _bench_e2e(args, D, w, seed, torch, fcp):
             if sessions[b] is None:
                 sessions[b] = CPAttention(D, w.cp, w.policy, hq, hkv, d, device=dev)
             sessions[b].set_plan(D, stream=s_in)
-            for h, g in zip(h_in, d_in[b]):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s_in)
+            # Q, K, V first: the forward needs only them; dO, the backward's
+            # input, follows while the forward runs.
+            for h, g in zip(h_in[:3], d_in[b][:3]):
                 g.copy_(h, non_blocking=True)
             in_ready[b].record(s_in)
+            d_in[b][3].copy_(h_in[3], non_blocking=True)
+            e1.record(s_in)
+            cin.append((e0, e1))
+            do_ready[b].record(s_in)
 
     def step(b):
         qd, kd, vd, dod = d_in[b]
@@ -652,20 +663,29 @@ def _bench_e2e(args, D, w, seed, torch, fcp):
         with torch.cuda.stream(s_comp):
             s_comp.wait_event(in_ready[b])
             s_comp.wait_event(out_done[b])          # results of two steps back have left
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            c0.record(s_comp)
             s = sessions[b]
             s.gather(kd, vd, stream=s_comp)
             s.forward(qd, kd, vd, out=o32[b], lse=lse[b], out_dtype=torch.float32, stream=s_comp)
             fcp.round_bf16(o32[b], o16, stream=s_comp)
             fwd_done[b].record(s_comp)
+            s_comp.wait_event(do_ready[b])
             s.backward(qd, kd, vd, o32[b], lse[b], dod, dq=dq, dk=dk, dv=dv, stream=s_comp)
+            c1.record(s_comp)
+            marks.append((c0, c1))
             comp_done[b].record(s_comp)
         with torch.cuda.stream(s_out):
             # O is final after the forward: it leaves while the backward runs.
             s_out.wait_event(fwd_done[b])
             h_out[b][0].copy_(o16, non_blocking=True)
             s_out.wait_event(comp_done[b])
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s_out)
             for g, h in zip(d_out[b][1:], h_out[b][1:]):
                 h.copy_(g, non_blocking=True)
+            e1.record(s_out)
+            cout.append((e0, e1))
             out_done[b].record(s_out)
 
     def run(n):
@@ -684,23 +704,40 @@ def _bench_e2e(args, D, w, seed, torch, fcp):
     # Timed runs of n steps each; with several runs the median is reported (one
     # host stall in a run -- allocation, page-in, another process -- otherwise
     # moves the whole figure).
-    runs = []
-    for _ in range(reps):
-        t0 = time.perf_counter()
-        run(n)
-        runs.append((time.perf_counter() - t0) / n)
+    runs, kern, bw_in, bw_out = [], [], [], []
+    h2d_bytes = sum(x.numel() * x.element_size() for x in h_in)
+    grad_bytes = sum(x.numel() * x.element_size() for x in h_out[0][1:])
+    clk = ClockSampler(torch.cuda.current_device())
+    with clk:
+        for _ in range(reps):
+            marks.clear()
+            cin.clear()
+            cout.clear()
+            t0 = time.perf_counter()
+            run(n)
+            runs.append((time.perf_counter() - t0) / n)
+            kern.append(sum(a.elapsed_time(b) for a, b in marks) / len(marks))
+            bw_in.append(statistics.median(h2d_bytes / (a.elapsed_time(b) * 1e6) for a, b in cin))
+            bw_out.append(statistics.median(grad_bytes / (a.elapsed_time(b) * 1e6) for a, b in cout))
     dt = sorted(runs)[len(runs) // 2]
     for s in sessions:
         if s is not None and s.device_status() != 0:
             raise RuntimeError("device status reports an error in the e2e leg")
-    h2d_bytes = sum(x.numel() * x.element_size() for x in h_in)
     d2h_bytes = sum(x.numel() * x.element_size() for x in h_out[0])
     r = {"value": round((14.0 * d * hq * pairs) / dt / 1e12, 2), "unit": UNIT, "ms_per_step": round(dt * 1e3, 3),
          "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes, "steps": n,
-         "includes": "per step: H2D of Q,K,V,dO; plan build + upload (buffers reused per buffer set); gather; fwd; "
+         "includes": "per step: H2D of Q,K,V then dO (the backward waits for dO only); plan build + upload "
+                     "(buffers reused per buffer set); gather; fwd; "
                      "rounding of O to bf16; bwd; D2H of O (bf16, as soon as the forward ends), dQ, dK, dV "
                      "(fp32) -- copies of neighbouring steps overlap this step's kernels on separate streams",
-         "runs_ms_per_step": [round(x * 1e3, 3) for x in runs]}
+         "runs_ms_per_step": [round(x * 1e3, 3) for x in runs],
+         # The kernels of a step (gather .. backward) on the compute stream, per
+         # run: the rest of ms_per_step is the first step's inputs and the last
+         # step's results, which nothing overlaps, plus any gap between steps.
+         "kernels_ms_per_step": [round(x, 3) for x in kern],
+         # Median copy rates of the run (Q, K, V, dO in; dQ, dK, dV out).
+         "h2d_GBps": [round(x, 1) for x in bw_in], "d2h_GBps": [round(x, 1) for x in bw_out],
+         "clocks": clk.summary()}
     del h_in, h_out, d_in, d_out, o32, lse, sessions
     return r
 
@@ -772,7 +809,7 @@ def main():
                     help="headline workload (1: 2K d=64, 2: 32K, 3: 128K, 4: 64K short docs, 5: 512K)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=3.0)
-    ap.add_argument("--e2e-steps", type=int, default=4,
+    ap.add_argument("--e2e-steps", type=int, default=6,
                     help="timed end-to-end steps on workloads above 200K tokens (one run of them; smaller "
                          "workloads take the median of three runs of max(4, steps / 2))")
     ap.add_argument("--legs", default="step,merge,ring,configs,shards,e2e,cpu",
