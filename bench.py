@@ -344,9 +344,11 @@ def run_gpu(args):
     policies = {}
     for pol in ("llama3", "perdoc", "wholedoc", "hybrid", "hybrid_tiles"):
         try:
-            ps = fcp.Plan(D, w.cp, pol).stats()
+            plan = fcp.Plan(D, w.cp, pol)
+            ps = plan.stats()
             policies[pol] = {"imbalance": round(ps["imbalance"], 4), "remote_rows": ps["remote_rows_total"],
-                             "eq4_tokens": ps["eq4_tokens"], "eq5_tokens": ps["eq5_tokens"]}
+                             "eq4_tokens": ps["eq4_tokens"], "eq5_tokens": ps["eq5_tokens"],
+                             "fwd_tiles": _tile_counts(plan, w.cp)}
         except fcp.FcpError as e:
             policies[pol] = {"error": str(e)}
     cpu = _cpu_baseline(args.cpu_seconds) if "cpu" in legs else None
@@ -394,6 +396,22 @@ def run_gpu(args):
     print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
+
+
+def _tile_counts(plan, cp):
+    """Forward 128 x 128 tiles over all shards, per head: visited without a
+    mask (full), visited with a per-element mask (partial), and skipped --
+    those a plain causal kernel over the packed sequence (key tiles 0 ..
+    the query tile's last row, no document mask) would add."""
+    visited = masked = causal = 0
+    for j in range(cp):
+        sh = plan.shard(j)
+        visited += sh["fwd_tiles"]
+        masked += sh["fwd_masked"]
+        for _, a, b in sh["pieces"]:
+            for q0 in range(a, b, 128):
+                causal += (min(q0 + 128, b) - 1) // 128 + 1
+    return {"full": visited - masked, "partial": masked, "skipped": causal - visited}
 
 
 def _bench_configs(torch, fcp, pk, dev):
