@@ -143,10 +143,18 @@ __global__ void __launch_bounds__(kMergeThreads)
           const float x = __shfl_sync(0xffffffffu, w, u * BP + ((b0 + k) % BP));
           wk[k] = b0 + k < B ? x : 0.f;
         }
+        // With more than one group of four parts, a group empty for every row
+        // of the pass is skipped by the whole warp (a vote: with d = 64 a pass
+        // covers two rows). Causal key blocks leave most rows' later groups
+        // empty.
+        if constexpr (BP > 4) {
+          if (__all_sync(0xffffffffu, wk[0] == 0.f && wk[1] == 0.f && wk[2] == 0.f && wk[3] == 0.f)) continue;
+        }
         // wk != 0 implies row < rows and part b0 + k non-empty.
+        const float4* opb = op + b0 * part_stride;
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          o[k] = wk[k] != 0.f ? __ldg(op + (b0 + k) * part_stride) : make_float4(0.f, 0.f, 0.f, 0.f);
+          o[k] = wk[k] != 0.f ? __ldg(opb + k * part_stride) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           acc.x = fmaf(wk[k], o[k].x, acc.x);
