@@ -129,12 +129,41 @@ __global__ void __launch_bounds__(kMergeThreads)
     // zero output and LSE -inf.
     w = (m == -INFINITY) ? 0.f : w * (1.f / tw);
     if (wb == 0 && r0 + wu < rows) lse_o[r0 + wu] = (m == -INFINITY) ? -INFINITY : m + logf(tw);
+    // Bit u * BP + b: part b of row u has a nonzero weight.
+    const uint32_t nz = __ballot_sync(0xffffffffu, w != 0.f);
 #pragma unroll 2
     for (int u0 = 0; u0 < G; u0 += kRowsPerPass) {
       const int u = u0 + sub;
       const int row = r0 + u;
       const float4* op = o_parts + ((int64_t)row * hq + h) * V + vec;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      if constexpr (kRowsPerPass == 1) {
+        // One row per pass (d = 128): the row's nonzero parts are the same in
+        // every lane, so empty parts cost neither a shuffle nor a load, and
+        // an empty group of four costs nothing.
+        const uint32_t rb = (nz >> (u * BP)) & (BP == 32 ? 0xffffffffu : ((1u << BP) - 1u));
+        for (int b0 = 0; b0 < B; b0 += 4) {
+          const uint32_t g = (rb >> b0) & 0xFu;
+          if (g == 0) continue;
+          float wk[4];
+          float4 o[4];
+          const float4* opb = op + b0 * part_stride;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) wk[k] = (g >> k) & 1u ? __shfl_sync(0xffffffffu, w, u * BP + b0 + k) : 0.f;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            o[k] = (g >> k) & 1u ? __ldg(opb + k * part_stride) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            acc.x = fmaf(wk[k], o[k].x, acc.x);
+            acc.y = fmaf(wk[k], o[k].y, acc.y);
+            acc.z = fmaf(wk[k], o[k].z, acc.z);
+            acc.w = fmaf(wk[k], o[k].w, acc.w);
+          }
+        }
+        if (row < rows) out[((int64_t)row * hq + h) * V + vec] = make_uint2(pack2(acc.x, acc.y), pack2(acc.z, acc.w));
+        continue;
+      }
       for (int b0 = 0; b0 < B; b0 += 4) {
         float wk[4];
         float4 o[4];
