@@ -239,6 +239,45 @@ def test_merge_kernel_against_oracle(cuda, B, d):
     assert np.max(np.abs(lg[fin] - l_ref[fin])) <= TOL_LSE
 
 
+def _merge_patterns(B, rows, hq, g):
+    """Emptiness patterns of B parts x rows (True = part has no visible key)."""
+    r = torch.arange(rows)
+    causal = torch.stack([r < b * rows // B for b in range(B)])           # contiguous key blocks
+    one = torch.ones(B, rows, dtype=torch.bool)                          # a single non-empty part per row
+    pick = torch.randint(0, B, (rows,), generator=g)
+    one[pick, r] = False
+    ends = torch.ones(B, rows, dtype=torch.bool)                         # first part (even rows) or last (odd)
+    ends[0, r % 2 == 0] = False
+    ends[B - 1, r % 2 == 1] = False
+    return {"causal": causal, "one": one, "ends": ends}
+
+
+@pytest.mark.parametrize("d,B", [(128, 5), (128, 8), (128, 13), (128, 16), (128, 32), (64, 8), (64, 11), (64, 16)])
+def test_merge_kernel_empty_part_patterns(cuda, d, B):
+    """Structured emptiness: whole groups of four parts empty for a row (or
+    for every row of a pass), the case the kernel skips without touching the
+    parts, beside rows where any single part is the only non-empty one."""
+    from context_document_masked_gb300 import fcp
+    g = torch.Generator().manual_seed(100 + B + d)
+    rows, hq = 389, 3
+    for name, empty in _merge_patterns(B, rows, hq, g).items():
+        o_parts = torch.randn(B, rows, hq, d, generator=g)
+        l_parts = torch.randn(B, hq, rows, generator=g) * 3
+        m = empty[:, None, :].expand(B, hq, rows)
+        l_parts[m] = float("-inf")
+        o_parts[m.permute(0, 2, 1)] = 0.0
+        out = torch.empty(rows, hq, d, dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty(hq, rows, dtype=torch.float32, device="cuda")
+        fcp.merge(o_parts.cuda(), l_parts.cuda(), out, lse)
+        torch.cuda.synchronize()
+        o_ref, l_ref = A.merge(o_parts.numpy(), l_parts.numpy())
+        assert _bf16_excess(out, o_ref) <= TOL_O, name
+        lg = lse.cpu().numpy()
+        assert np.array_equal(np.isneginf(lg), np.isneginf(l_ref)), name
+        fin = np.isfinite(l_ref)
+        assert np.max(np.abs(lg[fin] - l_ref[fin])) <= TOL_LSE, name
+
+
 BWD = [SMALL[0], SMALL[1], SMALL[3], SMALL[5], SMALL[6], SMALL[8], SMALL[9]]
 
 
