@@ -623,7 +623,8 @@ def _bench_e2e(args, D, w, seed, torch, fcp):
     """End to end through the public API, pipelined the way a training loop
     would run it: step i's inputs go host -> device on one stream while step
     i-1 computes (Q, K, V first, then dO, which only the backward reads), and
-    its results device -> host on a third stream while step i+1 computes. Every step copies all of its inputs in (Q, K, V, dO bf16) and
+    its results device -> host on a third stream while step i+1 computes.
+    Every step copies all of its inputs in (Q, K, V, dO bf16) and
     all of its results out (O rounded to bf16 -- the forward keeps its fp32 O
     on the device for the backward's D_i -- and dQ, dK, dV fp32), builds its
     plan and allocates its session buffers; buffers alternate between two sets,
