@@ -35,9 +35,9 @@ class CPAttention:
         received-key buffers and the workspace are kept when they are large
         enough and replaced otherwise. The previous plan's tables must no longer
         be in use by queued work on other streams."""
-        plan = fcp.Plan(doclens, self.cp, self.plan.policy, target_imbalance)
         if int(sum(int(x) for x in doclens)) != self.T:
             raise ValueError("set_plan: the token count differs from the session's")
+        plan = fcp.Plan(doclens, self.cp, self.plan.policy, target_imbalance)
         nbytes = plan.device_bytes()
         if self.plan_buf.numel() * 4 < nbytes:
             self.plan_buf = torch.empty(nbytes // 4, dtype=torch.int32, device=self.device)
