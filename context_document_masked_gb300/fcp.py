@@ -261,6 +261,50 @@ def _ptr(t):
     return C.c_void_p(0 if t is None else t.data_ptr())
 
 
+def _t(t, name, dtypes=None, shape=None):
+    """Checks a tensor before its raw pointer goes to the library, which cannot
+    see dtypes, strides or devices: a contiguous CUDA tensor of one of
+    `dtypes`, of `shape` (None entries free). Raises ValueError."""
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name}: expected a torch.Tensor, got {type(t).__name__}")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name}: must be a CUDA tensor (got {t.device})")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if dtypes is not None and t.dtype not in dtypes:
+        raise ValueError(f"{name}: dtype {t.dtype}, expected one of {tuple(str(x) for x in dtypes)}")
+    if shape is not None and (t.dim() != len(shape) or any(e is not None and e != x for e, x in zip(shape, t.shape))):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _qkv(q, k, v):
+    """Q [T][hq][d] and K, V [T][hkv][d], bf16; returns (T, hq, hkv, d)."""
+    import torch
+    _t(q, "q", (torch.bfloat16,), (None, None, None))
+    T, hq, d = q.shape
+    _t(k, "k", (torch.bfloat16,), (T, None, d))
+    _t(v, "v", (torch.bfloat16,), tuple(k.shape))
+    return T, hq, k.shape[1], d
+
+
+def _kbuf(kbuf, vbuf, dplan, hkv, d):
+    """The received-key buffers hold at least the plan's received rows (the
+    library writes and reads them by the plan, not by their size)."""
+    import torch
+    rows = max(1, int(dplan.c.total_remote_rows))
+    for t, n in ((kbuf, "kbuf"), (vbuf, "vbuf")):
+        _t(t, n, (torch.bfloat16,), (None, hkv, d))
+        if t.shape[0] < rows:
+            raise ValueError(f"{n}: {t.shape[0]} rows, the plan receives {rows}")
+
+
+def _out_lse(out, lse, T, hq, d):
+    import torch
+    _t(out, "out", (torch.bfloat16, torch.float32), (T, hq, d))
+    _t(lse, "lse", (torch.float32,), (hq, T))
+
+
 def dims(T: int, hq: int, hkv: int, d: int, scale: float = 0.0) -> Dims:
     return Dims(T, hq, hkv, d, scale)
 
@@ -270,6 +314,10 @@ def workspace_bytes(dm: Dims, plan: "Plan | None" = None) -> int:
 
 
 def gather_kv(k, v, dplan: DevicePlan, shard: int, kbuf, vbuf, stream=None):
+    import torch
+    _t(k, "k", (torch.bfloat16,), (None, None, None))
+    _t(v, "v", (torch.bfloat16,), tuple(k.shape))
+    _kbuf(kbuf, vbuf, dplan, k.shape[1], k.shape[2])
     _check(_lib.fcp_gather_kv(_ptr(k), _ptr(v), C.byref(dplan.c), shard, k.shape[1], k.shape[2],
                               _ptr(kbuf), _ptr(vbuf), _stream(stream)), "fcp_gather_kv")
 
@@ -277,8 +325,11 @@ def gather_kv(k, v, dplan: DevicePlan, shard: int, kbuf, vbuf, stream=None):
 def attn_fwd(q, k, v, kbuf, vbuf, dplan: DevicePlan, shard: int, out, lse, ws, kv_lo: int = 0,
              kv_hi: int | None = None, scale: float = 0.0, stream=None):
     import torch
-    T, hq, d = q.shape
-    dm = Dims(T, hq, k.shape[1], d, scale)
+    T, hq, hkv, d = _qkv(q, k, v)
+    _kbuf(kbuf, vbuf, dplan, hkv, d)
+    _out_lse(out, lse, T, hq, d)
+    _t(ws, "ws")
+    dm = Dims(T, hq, hkv, d, scale)
     out_dtype = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
     _check(_lib.fcp_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(kbuf), _ptr(vbuf), C.byref(dplan.c),
                              shard, kv_lo, T if kv_hi is None else kv_hi, dm, out_dtype, _ptr(out),
@@ -290,8 +341,11 @@ def attn_fwd_qk8(q, k, v, kbuf, vbuf, dplan: DevicePlan, shard: int, out, lse, w
                  kv_hi: int | None = None, scale: float = 0.0, stream=None):
     """fcp_attn_fwd_qk8: the forward with Q K^T on e4m3 copies of Q and K."""
     import torch
-    T, hq, d = q.shape
-    dm = Dims(T, hq, k.shape[1], d, scale)
+    T, hq, hkv, d = _qkv(q, k, v)
+    _kbuf(kbuf, vbuf, dplan, hkv, d)
+    _out_lse(out, lse, T, hq, d)
+    _t(ws, "ws")
+    dm = Dims(T, hq, hkv, d, scale)
     out_dtype = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
     _check(_lib.fcp_attn_fwd_qk8(_ptr(q), _ptr(k), _ptr(v), _ptr(kbuf), _ptr(vbuf), C.byref(dplan.c),
                                  shard, kv_lo, T if kv_hi is None else kv_hi, dm, out_dtype, _ptr(out),
@@ -301,6 +355,13 @@ def attn_fwd_qk8(q, k, v, kbuf, vbuf, dplan: DevicePlan, shard: int, out, lse, w
 
 def quant_e4m3(x, out, scale_out, scratch, stream=None):
     """fcp_quant_e4m3: out (uint8, x.numel() bytes) = e4m3(x * 2^k); scale_out[0] = 2^k."""
+    import torch
+    _t(x, "x", (torch.bfloat16,))
+    _t(out, "out", (torch.uint8,))
+    _t(scale_out, "scale_out", (torch.float32,))
+    _t(scratch, "scratch", (torch.int32,))
+    if out.numel() < x.numel() or scale_out.numel() < 1 or scratch.numel() < 1:
+        raise ValueError("quant_e4m3: out holds x.numel() bytes, scale_out and scratch one element each")
     _check(_lib.fcp_quant_e4m3(_ptr(x), x.numel(), _ptr(out), _ptr(scale_out), _ptr(scratch), _stream(stream)),
            "fcp_quant_e4m3")
 
@@ -311,8 +372,10 @@ def attn_fwd_ring(q, k, v, dplan: DevicePlan, shard: int, ring_step: int, out, l
     owners in ring order; ring_step -1 = all owners in one pass, s >= 0 = the
     partial result of ring step s."""
     import torch
-    T, hq, d = q.shape
-    dm = Dims(T, hq, k.shape[1], d, scale)
+    T, hq, hkv, d = _qkv(q, k, v)
+    _out_lse(out, lse, T, hq, d)
+    _t(ws, "ws")
+    dm = Dims(T, hq, hkv, d, scale)
     out_dtype = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
     _check(_lib.fcp_attn_fwd_ring(_ptr(q), _ptr(k), _ptr(v), C.byref(dplan.c), shard, ring_step, dm, out_dtype,
                                   _ptr(out), _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(),
@@ -325,8 +388,10 @@ def attn_fwd_noalloc(q, k, v, kbuf, vbuf, dplan: DevicePlan, shard: int, out, ls
     """fcp_attn_fwd_noalloc: the forward with the library's static scratch
     instead of a caller workspace (for callers that cannot allocate)."""
     import torch
-    T, hq, d = q.shape
-    dm = Dims(T, hq, k.shape[1], d, scale)
+    T, hq, hkv, d = _qkv(q, k, v)
+    _kbuf(kbuf, vbuf, dplan, hkv, d)
+    _out_lse(out, lse, T, hq, d)
+    dm = Dims(T, hq, hkv, d, scale)
     out_dtype = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
     _check(_lib.fcp_attn_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(kbuf), _ptr(vbuf), C.byref(dplan.c),
                                      shard, kv_lo, T if kv_hi is None else kv_hi, dm, out_dtype,
@@ -336,12 +401,26 @@ def attn_fwd_noalloc(q, k, v, kbuf, vbuf, dplan: DevicePlan, shard: int, out, ls
 
 def round_bf16(x, out, stream=None):
     """fcp_round_bf16: out (bf16, same element count) = x (fp32) rounded to nearest even."""
-    assert x.numel() == out.numel()
+    import torch
+    _t(x, "x", (torch.float32,))
+    _t(out, "out", (torch.bfloat16,))
+    if x.numel() != out.numel():
+        raise ValueError("round_bf16: x and out differ in element count")
     _check(_lib.fcp_round_bf16(_ptr(x), x.numel(), _ptr(out), _stream(stream)), "fcp_round_bf16")
 
 
-def merge(o_parts, lse_parts, out, lse_out, stream=None):
+def _merge_args(o_parts, lse_parts, out, lse_out):
+    import torch
+    _t(o_parts, "o_parts", (torch.float32,), (None, None, None, None))
     B, rows, hq, d = o_parts.shape
+    _t(lse_parts, "lse_parts", (torch.float32,), (B, hq, rows))
+    _t(out, "out", (torch.bfloat16,), (rows, hq, d))
+    _t(lse_out, "lse_out", (torch.float32,), (hq, rows))
+    return B, rows, hq, d
+
+
+def merge(o_parts, lse_parts, out, lse_out, stream=None):
+    B, rows, hq, d = _merge_args(o_parts, lse_parts, out, lse_out)
     _check(_lib.fcp_merge(_ptr(o_parts), _ptr(lse_parts), B, rows, hq, d, _ptr(out), _ptr(lse_out),
                           _stream(stream)), "fcp_merge")
 
@@ -354,6 +433,7 @@ def merge_ring(dplan: DevicePlan, o_parts, lse_parts, part_step, out, lse_out, s
     steps = np.ascontiguousarray(np.asarray(part_step, dtype=np.int32))
     if len(steps) != B or rows != dplan.c.T or tuple(lse_parts.shape) != (B, hq, rows):
         raise ValueError("merge_ring: one step tag per partial, each partial [T][hq][d] with T the plan's")
+    _merge_args(o_parts, lse_parts, out, lse_out)
     _check(_lib.fcp_merge_ring(C.byref(dplan.c), _ptr(o_parts), _ptr(lse_parts),
                                steps.ctypes.data_as(C.POINTER(C.c_int32)), len(steps), hq, d, _ptr(out),
                                _ptr(lse_out), _stream(stream)), "fcp_merge_ring")
@@ -362,8 +442,15 @@ def merge_ring(dplan: DevicePlan, o_parts, lse_parts, part_step, out, lse_out, s
 def attn_bwd(q, k, v, kbuf, vbuf, out, lse, dout, dplan: DevicePlan, shard: int, dq, dk, dv, ws,
              scale: float = 0.0, stream=None):
     import torch
-    T, hq, d = q.shape
-    dm = Dims(T, hq, k.shape[1], d, scale)
+    T, hq, hkv, d = _qkv(q, k, v)
+    _kbuf(kbuf, vbuf, dplan, hkv, d)
+    _out_lse(out, lse, T, hq, d)
+    _t(dout, "dout", (torch.bfloat16,), (T, hq, d))
+    _t(dq, "dq", (torch.float32,), (T, hq, d))
+    _t(dk, "dk", (torch.float32,), (T, hkv, d))
+    _t(dv, "dv", (torch.float32,), (T, hkv, d))
+    _t(ws, "ws")
+    dm = Dims(T, hq, hkv, d, scale)
     out_dtype = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
     _check(_lib.fcp_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(kbuf), _ptr(vbuf), _ptr(out), out_dtype,
                              _ptr(lse), _ptr(dout), C.byref(dplan.c), shard, dm, _ptr(dq), _ptr(dk),
@@ -372,6 +459,7 @@ def attn_bwd(q, k, v, kbuf, vbuf, out, lse, dout, dplan: DevicePlan, shard: int,
 
 
 def device_status(ws, stream=None) -> int:
+    _t(ws, "ws")
     return int(_lib.fcp_get_device_status(_ptr(ws), _stream(stream)))
 
 
@@ -381,6 +469,7 @@ def debug_set_wait_limit(ns: int):
 
 def debug_rescale_events(ws, stream=None) -> int:
     """Rescales of O after a later key tile since the last read (then cleared)."""
+    _t(ws, "ws")
     n = C.c_int64()
     _check(_lib.fcp_debug_rescale_events(_ptr(ws), _stream(stream), C.byref(n)), "fcp_debug_rescale_events")
     return int(n.value)
