@@ -240,6 +240,10 @@ int64_t fcp_workspace_bytes(fcp_dims dims, const fcp_plan_t* plan);
  * [rows][Hkv][d] bf16, in ascending kv_remote order. For shard == -1 the
  * shards' buffers are concatenated (shard j starts at its kbuf_base); for one
  * shard, kbuf row 0 is its first remote row. row_bytes = Hkv*d*2.
+ * Sizes (caller-owned, not checked here: the call takes no buffer sizes):
+ * kbuf and vbuf hold at least plan->total_remote_rows rows for shard == -1,
+ * or that shard's remote_rows (fcp_plan_shard) for one shard; the attention
+ * calls read them with the same layout.
  */
 int fcp_gather_kv(const void* k, const void* v, const fcp_dev_plan* plan, int32_t shard,
                   int32_t hkv, int32_t d, void* kbuf, void* vbuf, void* stream);
