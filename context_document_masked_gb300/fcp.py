@@ -288,11 +288,12 @@ def _qkv(q, k, v):
     return T, hq, k.shape[1], d
 
 
-def _kbuf(kbuf, vbuf, dplan, hkv, d):
-    """The received-key buffers hold at least the plan's received rows (the
-    library writes and reads them by the plan, not by their size)."""
+def _kbuf(kbuf, vbuf, dplan, shard, hkv, d):
+    """The received-key buffers hold at least the rows the plan sends to
+    `shard` (all shards' for -1): the library writes and reads them by the
+    plan, not by their size."""
     import torch
-    rows = max(1, int(dplan.c.total_remote_rows))
+    rows = max(1, dplan.remote_rows(shard))
     for t, n in ((kbuf, "kbuf"), (vbuf, "vbuf")):
         _t(t, n, (torch.bfloat16,), (None, hkv, d))
         if t.shape[0] < rows:
@@ -317,7 +318,7 @@ def gather_kv(k, v, dplan: DevicePlan, shard: int, kbuf, vbuf, stream=None):
     import torch
     _t(k, "k", (torch.bfloat16,), (None, None, None))
     _t(v, "v", (torch.bfloat16,), tuple(k.shape))
-    _kbuf(kbuf, vbuf, dplan, k.shape[1], k.shape[2])
+    _kbuf(kbuf, vbuf, dplan, shard, k.shape[1], k.shape[2])
     _check(_lib.fcp_gather_kv(_ptr(k), _ptr(v), C.byref(dplan.c), shard, k.shape[1], k.shape[2],
                               _ptr(kbuf), _ptr(vbuf), _stream(stream)), "fcp_gather_kv")
 
@@ -326,7 +327,7 @@ def attn_fwd(q, k, v, kbuf, vbuf, dplan: DevicePlan, shard: int, out, lse, ws, k
              kv_hi: int | None = None, scale: float = 0.0, stream=None):
     import torch
     T, hq, hkv, d = _qkv(q, k, v)
-    _kbuf(kbuf, vbuf, dplan, hkv, d)
+    _kbuf(kbuf, vbuf, dplan, shard, hkv, d)
     _out_lse(out, lse, T, hq, d)
     _t(ws, "ws")
     dm = Dims(T, hq, hkv, d, scale)
@@ -342,7 +343,7 @@ def attn_fwd_qk8(q, k, v, kbuf, vbuf, dplan: DevicePlan, shard: int, out, lse, w
     """fcp_attn_fwd_qk8: the forward with Q K^T on e4m3 copies of Q and K."""
     import torch
     T, hq, hkv, d = _qkv(q, k, v)
-    _kbuf(kbuf, vbuf, dplan, hkv, d)
+    _kbuf(kbuf, vbuf, dplan, shard, hkv, d)
     _out_lse(out, lse, T, hq, d)
     _t(ws, "ws")
     dm = Dims(T, hq, hkv, d, scale)
@@ -389,7 +390,7 @@ def attn_fwd_noalloc(q, k, v, kbuf, vbuf, dplan: DevicePlan, shard: int, out, ls
     instead of a caller workspace (for callers that cannot allocate)."""
     import torch
     T, hq, hkv, d = _qkv(q, k, v)
-    _kbuf(kbuf, vbuf, dplan, hkv, d)
+    _kbuf(kbuf, vbuf, dplan, shard, hkv, d)
     _out_lse(out, lse, T, hq, d)
     dm = Dims(T, hq, hkv, d, scale)
     out_dtype = OUT_F32 if out.dtype == torch.float32 else OUT_BF16
@@ -443,7 +444,7 @@ def attn_bwd(q, k, v, kbuf, vbuf, out, lse, dout, dplan: DevicePlan, shard: int,
              scale: float = 0.0, stream=None):
     import torch
     T, hq, hkv, d = _qkv(q, k, v)
-    _kbuf(kbuf, vbuf, dplan, hkv, d)
+    _kbuf(kbuf, vbuf, dplan, shard, hkv, d)
     _out_lse(out, lse, T, hq, d)
     _t(dout, "dout", (torch.bfloat16,), (T, hq, d))
     _t(dq, "dq", (torch.float32,), (T, hq, d))

@@ -88,3 +88,27 @@ def test_backward_and_merge_argument_checks(setup):
     torch.cuda.synchronize()
     assert torch.allclose(dq, dq2, rtol=1e-5, atol=1e-6)
     assert torch.allclose(dk, dk2, rtol=1e-5, atol=1e-6) and torch.allclose(dv, dv2, rtol=1e-5, atol=1e-6)
+
+
+def test_one_shard_buffers_sized_for_that_shard(setup):
+    """For one shard the received-key buffers need only that shard's received
+    rows (its row 0 is the shard's first); one row fewer is refused."""
+    from context_document_masked_gb300 import fcp
+    s, q, k, v, do = setup
+    s.gather(k, v)
+    o_all, l_all = s.forward(q, k, v, out_dtype=torch.float32)
+    for j in range(CP):
+        rows = s.dplan.remote_rows(j)
+        kb = torch.empty(max(1, rows), HKV, D, dtype=torch.bfloat16, device="cuda")
+        vb = torch.empty_like(kb)
+        fcp.gather_kv(k, v, s.dplan, j, kb, vb)
+        out = torch.zeros(T, HQ, D, dtype=torch.float32, device="cuda")
+        lse = torch.full((HQ, T), float("nan"), device="cuda")
+        fcp.attn_fwd(q, k, v, kb, vb, s.dplan, j, out, lse, s.ws)
+        torch.cuda.synchronize()
+        for _, a, b in s.plan.shard(j)["pieces"]:
+            assert torch.equal(out[a:b], o_all[a:b]) and torch.equal(lse[:, a:b], l_all[:, a:b])
+        if rows > 1:
+            with pytest.raises(ValueError):
+                fcp.attn_fwd(q, k, v, kb[:-1].contiguous(), vb[:-1].contiguous(), s.dplan, j, out, lse, s.ws)
+    assert s.device_status() == 0
